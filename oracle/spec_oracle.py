@@ -46,6 +46,7 @@ import numpy as np
 
 BOUNDARY_MARGIN = 1e-5   # a uniform this close to a decision boundary is a boundary case
 DEFAULT_EPS = 1e-6       # residual-mass threshold below which the fallback is used
+EPS_BAND = 0.5           # a residual mass within EPS_BAND * eps of eps is a boundary case
 
 FLAG_BAD_INPUT = 1       # a token, parent or row index out of range: request skipped
 FLAG_FALLBACK = 2        # the residual-mass fallback was used
@@ -199,7 +200,7 @@ def verify_chain_sampled(target: np.ndarray, draft: np.ndarray, draft_tokens: np
     if n_acc < gamma:
         w = np.maximum(P[n_acc] - Q[n_acc], 0.0)
         mass = w.sum()
-        if abs(mass - eps) < margin:
+        if abs(mass - eps) <= EPS_BAND * eps:
             res.boundary = True
         if mass <= eps:
             w = P[n_acc]
