@@ -1,0 +1,232 @@
+/*
+ * spec_verify.h — C ABI of the batched target-side verify-and-commit step of
+ * speculative decoding, built for one GB300 GPU (sm_103a).
+ *
+ * The step, as the pages define it:
+ *   * "10.6 投机解码：为什么“先猜后验”能加速" §10.6.1 (one round): the target
+ *     scores [x, d_1..d_gamma] in one forward, giving p_1..p_{gamma+1}; each
+ *     draft token d_k is tested left to right and accepted with probability
+ *     min(1, p_k(d_k)/q_k(d_k)); the first rejection draws one replacement
+ *     from norm(max(0, p_k - q_k)) and drops the rest; if every draft is
+ *     accepted a bonus token is drawn from p_{gamma+1}.
+ *   * "KV Cache 优化（四）：Speculative Decoding 投机解码" §4: the temperature /
+ *     top-k transform is part of p and q; at temperature 0 the rule becomes an
+ *     argmax match that emits the target's choice at the first mismatch.
+ *   * "投机推理：小模型搭树，大模型一次验证", Validation / 接受过程: a draft tree
+ *     is verified by walking one root-to-leaf path, never summing matches
+ *     across branches; §10.6.3 Table 10-17: each node attends to its
+ *     ancestors only and its position id is its depth.
+ *   * "KV Cache 优化（四）" §6 and §10.6.3: the accepted prefix's temporary
+ *     K/V is committed at one boundary in every layer, the commit length
+ *     advances, rejected slots are rolled back without copying blocks.
+ *
+ * Conventions for every entry point
+ *   * All pointers named "device" are CUDA device (or managed) pointers; the
+ *     argument structs themselves live in host memory and are read during
+ *     the call only.
+ *   * The caller owns every buffer, including the workspace.  The library
+ *     never allocates, never synchronises the stream and never creates
+ *     streams; each call enqueues its kernels on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream) and returns.
+ *   * Host-detectable problems return SPEC_ERR_INVALID_ARG or
+ *     SPEC_ERR_UNSUPPORTED before anything is enqueued; a failed launch
+ *     returns SPEC_ERR_CUDA.  Problems that only the data shows (a token,
+ *     node or block id out of range; a row whose kept logits are all -inf)
+ *     are found on the device: the request's flags word and the workspace's
+ *     sticky status word get a SPEC_FLAG_* bit, the request's outputs are
+ *     not written except n_acc = n_out = 0 (and for a commit, nothing is
+ *     copied and its length does not advance).  No kernel traps or waits on
+ *     another block.
+ *   * Logits must not contain NaN or +inf (-inf is allowed and means "never").
+ *   * The workspace must be at least spec_workspace_bytes(...) bytes, 256-byte
+ *     aligned and zero-filled before its first use; every call leaves it
+ *     zeroed again (except the sticky status word).  Calls sharing one
+ *     workspace must be ordered on one stream.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG 1
+#define SPEC_ERR_UNSUPPORTED 2
+#define SPEC_ERR_CUDA 3
+
+/* logits element types */
+#define SPEC_DTYPE_BF16 0
+#define SPEC_DTYPE_F32 1
+
+/* per-request flag bits (flags[b]) and sticky status-word bits */
+#define SPEC_FLAG_BAD_INPUT 1u  /* token / node / slot / block id out of range: request skipped */
+#define SPEC_FLAG_FALLBACK 2u   /* residual mass <= fallback_eps: the draw used p_k itself */
+#define SPEC_FLAG_BAD_ROW 4u    /* every kept logit of a row is -inf: request skipped */
+
+/* workspace kinds for spec_workspace_bytes */
+#define SPEC_WS_CHAIN 0 /* n = gamma */
+#define SPEC_WS_TREE 1  /* n = R (logits rows per request) */
+#define SPEC_WS_COMMIT 2
+
+/*
+ * Chain verification, sampled (temperature > 0) or greedy (temperature == 0).
+ *
+ * Rows: target row (b, k), k = 0..gamma, holds p_{k+1}'s logits at
+ *   target_logits + (b*(gamma+1) + k) * target_row_stride elements;
+ *   draft row (b, k), k = 0..gamma-1, holds q_{k+1}'s logits at
+ *   draft_logits + (b*gamma + k) * draft_row_stride.  Strides are in
+ *   elements and >= V; any alignment of the element type is accepted (16-byte
+ *   aligned rows are fastest).
+ * Transform ("KV Cache 优化（四）" §4): top-k keeps every token whose raw
+ *   logit is >= the k-th largest (ties at the threshold are all kept;
+ *   top_k == 0 or >= V keeps all), then p_i = exp((l_i - m)/T) / sum over
+ *   the kept set.  The draft rows get the same transform.
+ * Acceptance (§10.6.1): d_k is accepted iff uniforms[b][k-1] < a_k with
+ *   a_k = min(1, p_k(d_k)/q_k(d_k)) (a_k = 1 if q_k(d_k) = 0 < p_k(d_k), 0 if
+ *   both are 0).  At the first rejection k: w = max(0, p_k - q_k); if
+ *   sum(w) <= fallback_eps, w = p_k (SPEC_FLAG_FALLBACK); the emitted token
+ *   is the smallest i with C_i > uniforms[b][gamma] * C_total, C_i = the
+ *   running sum of w in token order.  If all are accepted the same rule
+ *   draws from p_{gamma+1}.  Exactly one final uniform is used per round.
+ * Greedy (temperature == 0): the argmax of each target row (lowest index on
+ *   ties) is compared with d_k; draft_logits and uniforms may be NULL.
+ *
+ * Outputs (device): n_acc[b] in 0..gamma; out_tokens[b][0..n_out-1] = the
+ *   accepted drafts then the drawn token (row stride gamma+1); n_out[b] =
+ *   n_acc[b] + 1.  Optional (NULL = not written): accept_prob[b][k] = a_k for
+ *   every k (sampled only); residual_mass[b][k] = sum max(0, p_k - q_k) for
+ *   every k (sampled only; costs a second on-chip pass over every row pair);
+ *   flags[b].
+ */
+typedef struct SpecChainArgs {
+    int32_t B, gamma, V, dtype;
+    const void *target_logits;  /* device, [B*(gamma+1)] rows of V logits */
+    int64_t target_row_stride;  /* elements */
+    const void *draft_logits;   /* device, [B*gamma] rows; NULL when greedy */
+    int64_t draft_row_stride;   /* elements */
+    const int32_t *draft_tokens; /* device, int32 [B][gamma] */
+    const float *uniforms;      /* device, f32 [B][gamma+1] in [0,1); NULL when greedy */
+    float temperature;          /* 0 = greedy; otherwise > 0 and finite */
+    int32_t top_k;              /* 0 = off */
+    float fallback_eps;         /* >= 0; 1e-6 is the documented default */
+    int32_t *n_acc;             /* device out [B] */
+    int32_t *out_tokens;        /* device out [B][gamma+1] */
+    int32_t *n_out;             /* device out [B] */
+    float *accept_prob;         /* device out [B][gamma] or NULL */
+    float *residual_mass;       /* device out [B][gamma] or NULL */
+    uint32_t *flags;            /* device out [B] or NULL */
+} SpecChainArgs;
+
+int spec_verify_chain(const SpecChainArgs *args, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/*
+ * Greedy tree verification ("投机推理：小模型搭树，大模型一次验证",
+ * Validation and 接受过程：沿一条路径走; mask and positions from §10.6.3
+ * Table 10-17).
+ *
+ * Nodes: node 0 is the root (the last emitted token; its K/V is slot 0);
+ *   nodes 1..N are drafts with node_token[b][i-1] and node_parent[b][i-1]
+ *   (0 <= parent < i, so ids are in breadth-first or any topological order).
+ *   row_of_node[b][i] is the logits row scored at node i (-1 = none); row r
+ *   of request b is at logits + (b*R + r) * row_stride.
+ * Walk: from the root, while the current node has a row, take that row's
+ *   argmax t (lowest index on ties) and move to the lowest-id child of the
+ *   current node whose token is t; if none matches, t is emitted and the
+ *   walk ends; a node without a row ends the walk with no extra token.
+ * Outputs (device): path[b][0..n_acc-1] = accepted node ids (row stride N);
+ *   n_acc[b]; out_tokens[b][0..n_out-1] = their tokens then the emitted
+ *   token if any (row stride N+1); n_out[b].  Optional: tree_mask[b][i][w]
+ *   (row stride W = ceil((N+1)/32) words; bit j of word j/32 set iff node j is
+ *   node i or an ancestor of it); pos[b][i] = committed_len[b] + depth(i)
+ *   (committed_len is then required); commit_slots[b][0..n_commit-1] = root
+ *   then the path (row stride N+1) and n_commit[b] = n_acc[b] + 1, ready for
+ *   spec_commit_kv; flags[b].
+ */
+typedef struct SpecTreeArgs {
+    int32_t B, N, R, V, dtype;
+    const void *logits;          /* device, [B*R] rows */
+    int64_t row_stride;          /* elements, >= V */
+    const int32_t *node_token;   /* device, int32 [B][N] */
+    const int32_t *node_parent;  /* device, int32 [B][N] */
+    const int32_t *row_of_node;  /* device, int32 [B][N+1] */
+    const int32_t *committed_len; /* device, int32 [B]; may be NULL if pos == NULL */
+    int32_t *path;               /* device out [B][N] */
+    int32_t *n_acc;              /* device out [B] */
+    int32_t *out_tokens;         /* device out [B][N+1] */
+    int32_t *n_out;              /* device out [B] */
+    uint32_t *tree_mask;         /* device out [B][N+1][W] or NULL */
+    int32_t *pos;                /* device out [B][N+1] or NULL */
+    int32_t *commit_slots;       /* device out [B][N+1] or NULL */
+    int32_t *n_commit;           /* device out [B] or NULL */
+    uint32_t *flags;             /* device out [B] or NULL */
+} SpecTreeArgs;
+
+int spec_verify_tree(const SpecTreeArgs *args, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * KV commit and rollback ("KV Cache 优化（四）" §6; §10.6.3).
+ *
+ * temp_kv holds each request's temporary K/V: [B][L][2][S][H][D] elements of
+ *   elem_bytes bytes (2 for bf16), K at index 0 and V at 1 of the third
+ *   dimension.  cache is the paged cache [L][2][num_blocks][block_size][H][D];
+ *   block_table[b][j] (row stride max_blocks) is the cache block holding
+ *   request b's positions j*block_size .. j*block_size+block_size-1.
+ * For i < n_slots[b], slot slots[b][i] (row stride slots_stride; NULL means
+ *   slot i) is copied to position committed_len[b] + i in every layer, K and
+ *   V alike; then committed_len[b] += n_slots[b].  Slots past n_slots are
+ *   never copied: rolling back a rejected draft is not advancing past it.
+ *   blocks_in_use[b] (optional) = ceil(new length / block_size): blocks of
+ *   the table past it may be released by the caller.
+ * Chain rounds pass slots = NULL and n_slots = n_out from spec_verify_chain
+ *   (slot 0 = the last emitted token's K/V, slots 1..n_acc = the accepted
+ *   drafts); tree rounds pass commit_slots / n_commit from spec_verify_tree.
+ * H*D*elem_bytes must be a multiple of 16.  The whole request is skipped
+ *   (SPEC_FLAG_BAD_INPUT) if any slot id is outside [0,S), n_slots outside
+ *   [0,S], the new length exceeds max_blocks*block_size or a block id it
+ *   needs is outside [0,num_blocks).
+ */
+typedef struct SpecCommitArgs {
+    int32_t B, L, H, D, S, block_size, elem_bytes;
+    const void *temp_kv;         /* device, [B][L][2][S][H][D] */
+    void *cache;                 /* device, [L][2][num_blocks][block_size][H][D] */
+    int64_t num_blocks;
+    const int32_t *block_table;  /* device, int32 [B][max_blocks] */
+    int32_t max_blocks;
+    const int32_t *slots;        /* device, int32 [B][slots_stride] or NULL (identity) */
+    int32_t slots_stride;
+    const int32_t *n_slots;      /* device, int32 [B] */
+    int32_t *committed_len;      /* device, int32 [B], in/out */
+    int32_t *blocks_in_use;      /* device out [B] or NULL */
+    uint32_t *flags;             /* device out [B] or NULL (bits are OR-ed in) */
+} SpecCommitArgs;
+
+int spec_commit_kv(const SpecCommitArgs *args, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Workspace bytes for a call of the given kind (n = gamma for SPEC_WS_CHAIN,
+ * R for SPEC_WS_TREE, ignored for SPEC_WS_COMMIT).  Returns 0 for an unknown
+ * kind or negative sizes. */
+size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V);
+
+/* Reads (and clears) the workspace's sticky status word: enqueues a copy on
+ * `stream`, synchronises that stream, then enqueues the clear.  This is the
+ * one call that synchronises. */
+int spec_get_status(void *workspace, void *stream, uint32_t *host_flags);
+
+/* Human-readable text for a return code. */
+const char *spec_error_string(int code);
+
+/* Text of the last CUDA error a call of this library saw on this thread. */
+const char *spec_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

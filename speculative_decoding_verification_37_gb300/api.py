@@ -1,0 +1,117 @@
+"""Convenience layer over the C ABI: allocates outputs and workspaces with
+torch and calls the library.  No arithmetic of the method happens here."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _lib as L
+
+_WORKSPACES: Dict[Tuple, torch.Tensor] = {}
+
+
+def workspace(kind: int, B: int, n: int, V: int, device) -> torch.Tensor:
+    """A cached zero-filled workspace for (device, kind, B, n).  Every call
+    leaves it zeroed, so it is reused without clearing; calls that share it
+    must be ordered on one stream."""
+    dev = torch.device(device)
+    key = (dev.type, dev.index, kind, B, n)
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        ws = L.new_workspace(kind, B, n, V, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+@dataclass
+class ChainOut:
+    n_acc: torch.Tensor                   # int32 [B]
+    out_tokens: torch.Tensor              # int32 [B, gamma+1]
+    n_out: torch.Tensor                   # int32 [B]
+    accept_prob: Optional[torch.Tensor]   # f32 [B, gamma]
+    residual_mass: Optional[torch.Tensor] # f32 [B, gamma]
+    flags: torch.Tensor                   # uint32 stored as int32 [B]
+
+
+def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int,
+                 temperature: float, draft: Optional[torch.Tensor] = None,
+                 uniforms: Optional[torch.Tensor] = None, top_k: int = 0,
+                 fallback_eps: float = 1e-6, accept_prob: bool = True,
+                 residual_mass: bool = False, ws: Optional[torch.Tensor] = None,
+                 stream=None) -> ChainOut:
+    """target [B*(gamma+1), V], draft [B*gamma, V] (bf16 or f32, rows may be
+    strided), draft_tokens int32 [B, gamma], uniforms f32 [B, gamma+1]."""
+    dev = target.device
+    V = target.shape[-1]
+    B = target.shape[0] // (gamma + 1)
+    sampled = temperature > 0
+    out = ChainOut(
+        n_acc=torch.empty(B, dtype=torch.int32, device=dev),
+        out_tokens=torch.full((B, gamma + 1), -1, dtype=torch.int32, device=dev),
+        n_out=torch.empty(B, dtype=torch.int32, device=dev),
+        accept_prob=torch.empty((B, gamma), dtype=torch.float32, device=dev)
+        if (sampled and accept_prob) else None,
+        residual_mass=torch.empty((B, gamma), dtype=torch.float32, device=dev)
+        if (sampled and residual_mass) else None,
+        flags=torch.zeros(B, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(L.SPEC_WS_CHAIN, B, gamma, V, dev)
+    L.spec_verify_chain(target_logits=target, draft_tokens=draft_tokens, n_acc=out.n_acc,
+                        out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws, gamma=gamma,
+                        temperature=temperature, draft_logits=draft, uniforms=uniforms,
+                        top_k=top_k, fallback_eps=fallback_eps, accept_prob=out.accept_prob,
+                        residual_mass=out.residual_mass, flags=out.flags, stream=stream)
+    return out
+
+
+@dataclass
+class TreeOut:
+    path: torch.Tensor          # int32 [B, N]
+    n_acc: torch.Tensor         # int32 [B]
+    out_tokens: torch.Tensor    # int32 [B, N+1]
+    n_out: torch.Tensor         # int32 [B]
+    tree_mask: torch.Tensor     # int32 view of uint32 [B, N+1, W]
+    pos: torch.Tensor           # int32 [B, N+1]
+    commit_slots: torch.Tensor  # int32 [B, N+1]
+    n_commit: torch.Tensor      # int32 [B]
+    flags: torch.Tensor         # int32 [B]
+
+
+def verify_tree(logits: torch.Tensor, node_token: torch.Tensor, node_parent: torch.Tensor,
+                row_of_node: torch.Tensor, committed_len: torch.Tensor, *, R: int,
+                ws: Optional[torch.Tensor] = None, stream=None) -> TreeOut:
+    dev = logits.device
+    V = logits.shape[-1]
+    B = logits.shape[0] // R
+    N = node_token.shape[-1]
+    W = (N + 1 + 31) // 32
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = TreeOut(path=torch.full((B, N), -1, **i32), n_acc=torch.empty(B, **i32),
+                  out_tokens=torch.full((B, N + 1), -1, **i32), n_out=torch.empty(B, **i32),
+                  tree_mask=torch.zeros((B, N + 1, W), **i32), pos=torch.empty((B, N + 1), **i32),
+                  commit_slots=torch.full((B, N + 1), -1, **i32), n_commit=torch.empty(B, **i32),
+                  flags=torch.zeros(B, **i32))
+    if ws is None:
+        ws = workspace(L.SPEC_WS_TREE, B, R, V, dev)
+    L.spec_verify_tree(logits=logits, R=R, node_token=node_token, node_parent=node_parent,
+                       row_of_node=row_of_node, path=out.path, n_acc=out.n_acc,
+                       out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws,
+                       committed_len=committed_len, tree_mask=out.tree_mask, pos=out.pos,
+                       commit_slots=out.commit_slots, n_commit=out.n_commit, flags=out.flags,
+                       stream=stream)
+    return out
+
+
+def commit_kv(temp_kv: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+              n_slots: torch.Tensor, committed_len: torch.Tensor, *, block_size: int,
+              slots: Optional[torch.Tensor] = None, blocks_in_use: Optional[torch.Tensor] = None,
+              flags: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+              stream=None) -> None:
+    """Commits in place: cache and committed_len are updated on the device."""
+    if ws is None:
+        ws = workspace(L.SPEC_WS_COMMIT, temp_kv.shape[0], 0, 0, temp_kv.device)
+    L.spec_commit_kv(temp_kv=temp_kv, cache=cache, block_table=block_table, n_slots=n_slots,
+                     committed_len=committed_len, block_size=block_size, workspace=ws,
+                     slots=slots, blocks_in_use=blocks_in_use, flags=flags, stream=stream)

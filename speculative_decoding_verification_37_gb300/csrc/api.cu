@@ -1,0 +1,275 @@
+// C ABI of the verify-and-commit library: argument validation, workspace
+// layout, launch configuration.  No allocation, no synchronisation (except
+// spec_get_status, which says so), no stream creation.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "kernels.h"
+#include "spec_verify.h"
+
+using namespace specv;
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return SPEC_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t esize(int dtype) { return dtype == SPEC_DTYPE_BF16 ? 2 : 4; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n > 0 ? n : 148;
+}
+
+// Slices per row: about 64 KiB of logits per block, at most 8 (cluster limit).
+int slices_for(int V, int dtype, int max_slices) {
+    const int64_t bytes = (int64_t)V * (int64_t)esize(dtype);
+    int64_t c = (bytes + 65535) / 65536;
+    if (c < 1) c = 1;
+    if (c > max_slices) c = max_slices;
+    return (int)c;
+}
+
+int slice_len(int V, int c) {
+    int s = (V + c - 1) / c;
+    return (s + 7) & ~7;  // whole 16-byte vectors for both element types
+}
+
+struct Ws {
+    unsigned *status;
+    unsigned *counters;
+    void *data;
+};
+
+Ws ws_layout(void *ws, int B) {
+    char *base = static_cast<char *>(ws);
+    Ws w;
+    w.status = reinterpret_cast<unsigned *>(base);
+    w.counters = reinterpret_cast<unsigned *>(base + kWsHeader);
+    w.data = base + kWsHeader + ws_align((size_t)B * sizeof(unsigned));
+    return w;
+}
+
+}  // namespace
+
+extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V) {
+    (void)V;
+    if (B < 0 || n < 0) return 0;
+    const size_t head = kWsHeader + ws_align((size_t)B * sizeof(unsigned));
+    switch (kind) {
+    case SPEC_WS_CHAIN: {
+        const size_t rows = (size_t)B * ((size_t)n + 1);
+        const size_t rec = rows * sizeof(PosRec);
+        const size_t keys = rows * sizeof(unsigned long long);
+        return head + ws_align(rec > keys ? rec : keys);
+    }
+    case SPEC_WS_TREE:
+        return head + ws_align((size_t)B * (size_t)n * sizeof(unsigned long long));
+    case SPEC_WS_COMMIT:
+        return 2 * kWsHeader;
+    default:
+        return 0;
+    }
+}
+
+extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->B < 0 || a->gamma < 0 || a->gamma > 4096 || a->V < 1) return SPEC_ERR_INVALID_ARG;
+    if (a->dtype != SPEC_DTYPE_BF16 && a->dtype != SPEC_DTYPE_F32) return SPEC_ERR_INVALID_ARG;
+    if (!(a->temperature >= 0.0f) || !std::isfinite(a->temperature)) return SPEC_ERR_INVALID_ARG;
+    if (a->top_k < 0 || !(a->fallback_eps >= 0.0f) || !std::isfinite(a->fallback_eps))
+        return SPEC_ERR_INVALID_ARG;
+    if (a->B == 0) return SPEC_OK;
+    const bool greedy = a->temperature == 0.0f;
+    if (!a->target_logits || a->target_row_stride < a->V) return SPEC_ERR_INVALID_ARG;
+    if (!a->n_acc || !a->out_tokens || !a->n_out) return SPEC_ERR_INVALID_ARG;
+    if (a->gamma > 0 && !a->draft_tokens) return SPEC_ERR_INVALID_ARG;
+    if (!greedy) {
+        if (!a->uniforms) return SPEC_ERR_INVALID_ARG;
+        if (a->gamma > 0 && (!a->draft_logits || a->draft_row_stride < a->V)) return SPEC_ERR_INVALID_ARG;
+    }
+    const size_t es = esize(a->dtype);
+    if (!aligned(a->target_logits, es) || (a->draft_logits && !aligned(a->draft_logits, es)))
+        return SPEC_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)a->B * (a->gamma + 1);
+    if (!workspace || !aligned(workspace, 256) ||
+        ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
+        return SPEC_ERR_INVALID_ARG;
+    const Ws w = ws_layout(workspace, a->B);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (greedy) {
+        ArgmaxParams p = {};
+        p.rows = a->target_logits;
+        p.stride = a->target_row_stride;
+        p.V = a->V;
+        p.slices = slices_for(a->V, a->dtype, 64);
+        p.slice_len = slice_len(a->V, p.slices);
+        p.rows_per_req = a->gamma + 1;
+        p.keys = static_cast<unsigned long long *>(w.data);
+        p.counters = w.counters;
+        p.status = w.status;
+        p.mode = 0;
+        p.gamma = a->gamma;
+        p.tokens = a->draft_tokens;
+        p.n_acc = a->n_acc;
+        p.out_tokens = a->out_tokens;
+        p.n_out = a->n_out;
+        p.flags = a->flags;
+        if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+        e = launch_argmax_verify(p, a->dtype, (int)rows, s);
+    } else {
+        SampleParams p = {};
+        p.B = a->B;
+        p.gamma = a->gamma;
+        p.V = a->V;
+        p.c = slices_for(a->V, a->dtype, 8);
+        p.Vs = slice_len(a->V, p.c);
+        p.target = a->target_logits;
+        p.tstride = a->target_row_stride;
+        p.draft = a->draft_logits;
+        p.dstride = a->draft_row_stride;
+        p.tokens = a->draft_tokens;
+        p.unif = a->uniforms;
+        p.c2 = (float)(1.4426950408889634 / (double)a->temperature);
+        p.top_k = (a->top_k >= a->V) ? 0 : a->top_k;
+        p.eps = a->fallback_eps;
+        p.n_acc = a->n_acc;
+        p.out_tokens = a->out_tokens;
+        p.n_out = a->n_out;
+        p.accept_prob = a->accept_prob;
+        p.resid = a->residual_mass;
+        p.flags = a->flags;
+        p.status = w.status;
+        p.counters = w.counters;
+        p.recs = static_cast<PosRec *>(w.data);
+        if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
+        if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+        e = launch_chain_sample(p, a->dtype, s);
+    }
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
+extern "C" int spec_verify_tree(const SpecTreeArgs *a, void *workspace, size_t ws_bytes, void *stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->B < 0 || a->N < 0 || a->N > 1023 || a->R < 1 || a->V < 1) return SPEC_ERR_INVALID_ARG;
+    if (a->dtype != SPEC_DTYPE_BF16 && a->dtype != SPEC_DTYPE_F32) return SPEC_ERR_INVALID_ARG;
+    if (a->B == 0) return SPEC_OK;
+    if (!a->logits || a->row_stride < a->V || !aligned(a->logits, esize(a->dtype)))
+        return SPEC_ERR_INVALID_ARG;
+    if ((a->N > 0 && (!a->node_token || !a->node_parent || !a->path)) || !a->row_of_node)
+        return SPEC_ERR_INVALID_ARG;
+    if (!a->n_acc || !a->out_tokens || !a->n_out) return SPEC_ERR_INVALID_ARG;
+    if (a->pos && !a->committed_len) return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) ||
+        ws_bytes < spec_workspace_bytes(SPEC_WS_TREE, a->B, a->R, a->V))
+        return SPEC_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)a->B * a->R;
+    const Ws w = ws_layout(workspace, a->B);
+    ArgmaxParams p = {};
+    p.rows = a->logits;
+    p.stride = a->row_stride;
+    p.V = a->V;
+    p.slices = slices_for(a->V, a->dtype, 64);
+    p.slice_len = slice_len(a->V, p.slices);
+    p.rows_per_req = a->R;
+    p.keys = static_cast<unsigned long long *>(w.data);
+    p.counters = w.counters;
+    p.status = w.status;
+    p.mode = 1;
+    p.N = a->N;
+    p.R = a->R;
+    p.node_token = a->node_token;
+    p.node_parent = a->node_parent;
+    p.row_of_node = a->row_of_node;
+    p.committed_len = a->committed_len;
+    p.path = a->path;
+    p.mask = a->tree_mask;
+    p.pos = a->pos;
+    p.commit_slots = a->commit_slots;
+    p.n_commit = a->n_commit;
+    p.n_acc = a->n_acc;
+    p.out_tokens = a->out_tokens;
+    p.n_out = a->n_out;
+    p.flags = a->flags;
+    if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_argmax_verify(p, a->dtype, (int)rows, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
+extern "C" int spec_commit_kv(const SpecCommitArgs *a, void *workspace, size_t ws_bytes, void *stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->B < 0 || a->B > 32768 || a->L < 1 || a->H < 1 || a->D < 1 || a->S < 1 ||
+        a->block_size < 1 || a->num_blocks < 1 || a->max_blocks < 1)
+        return SPEC_ERR_INVALID_ARG;
+    if (a->elem_bytes != 1 && a->elem_bytes != 2 && a->elem_bytes != 4) return SPEC_ERR_INVALID_ARG;
+    const int64_t unit = (int64_t)a->H * a->D * a->elem_bytes;
+    if (unit % 16 != 0 || unit > (1 << 20)) return SPEC_ERR_UNSUPPORTED;
+    if (a->B == 0) return SPEC_OK;
+    if (!a->temp_kv || !a->cache || !a->block_table || !a->n_slots || !a->committed_len)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(a->temp_kv, 16) || !aligned(a->cache, 16)) return SPEC_ERR_INVALID_ARG;
+    if (a->slots && a->slots_stride < 1) return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < spec_workspace_bytes(SPEC_WS_COMMIT, a->B, 0, 0))
+        return SPEC_ERR_INVALID_ARG;
+    char *base = static_cast<char *>(workspace);
+    CommitParams p = {};
+    p.B = a->B;
+    p.L = a->L;
+    p.S = a->S;
+    p.bs = a->block_size;
+    p.unit_bytes = (int)unit;
+    p.max_blocks = a->max_blocks;
+    p.slots_stride = a->slots_stride;
+    p.temp = static_cast<const char *>(a->temp_kv);
+    p.cache = static_cast<char *>(a->cache);
+    p.nb = a->num_blocks;
+    p.table = a->block_table;
+    p.slots = a->slots;
+    p.n_slots = a->n_slots;
+    p.len = a->committed_len;
+    p.blocks_in_use = a->blocks_in_use;
+    p.flags = a->flags;
+    p.status = reinterpret_cast<unsigned *>(base);
+    p.counter = reinterpret_cast<unsigned *>(base + kWsHeader);
+    // enough warps to cover every SM a few times; the kernel strides over units
+    const int64_t max_units = (int64_t)a->B * a->S * a->L * 2;
+    const int warps_per_block = commit_threads() / 32;
+    int64_t grid = (max_units + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)sm_count() * 4;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const cudaError_t e = launch_commit_kv(p, (int)grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
+extern "C" int spec_get_status(void *workspace, void *stream, uint32_t *host_flags) {
+    if (!workspace || !host_flags) return SPEC_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
+extern "C" const char *spec_error_string(int code) {
+    switch (code) {
+    case SPEC_OK: return "success";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    default: return "unknown error code";
+    }
+}
+
+extern "C" const char *spec_last_cuda_error(void) { return g_cuda_err; }

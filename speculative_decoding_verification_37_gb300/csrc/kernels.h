@@ -1,0 +1,78 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+// Workspace layout shared by every verify kind: a sticky status word, one
+// arrival counter per request, then per-row argmax keys or per-position
+// records.  All of it starts zeroed and is left zeroed (except the status).
+constexpr size_t kWsHeader = 256;
+inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct PosRec {      // one chain position's outcome, written by its cluster
+    float a;         // acceptance probability a_k
+    float z;         // residual mass sum max(0, p_k - q_k)
+    int token;       // drawn token if this position rejected (or is the bonus row)
+    unsigned info;   // REC_* bits
+};
+constexpr unsigned REC_ACCEPT = 1u, REC_BAD_INPUT = 2u, REC_BAD_ROW = 4u, REC_FALLBACK = 8u;
+
+struct ArgmaxParams {
+    const void *rows;
+    int64_t stride;
+    int V, slices, slice_len, rows_per_req;
+    unsigned long long *keys;  // [B*rows_per_req]
+    unsigned *counters;        // [B]
+    unsigned *status;
+    int mode;                  // 0 = greedy chain, 1 = tree
+    // chain
+    int gamma;
+    const int *tokens;
+    // tree
+    int N, R;
+    const int *node_token, *node_parent, *row_of_node, *committed_len;
+    int *path, *pos, *commit_slots, *n_commit;
+    uint32_t *mask;
+    // outputs shared by both
+    int *n_acc, *out_tokens, *n_out;
+    unsigned *flags;
+};
+
+struct SampleParams {
+    int B, gamma, V, c, Vs;
+    const void *target;
+    int64_t tstride;
+    const void *draft;
+    int64_t dstride;
+    const int *tokens;
+    const float *unif;
+    float c2;      // log2(e) / temperature
+    int top_k;     // 0 = keep all
+    float eps;
+    int *n_acc, *out_tokens, *n_out;
+    float *accept_prob, *resid;
+    unsigned *flags;
+    unsigned *status, *counters;
+    PosRec *recs;  // [B*(gamma+1)]
+};
+
+struct CommitParams {
+    int B, L, S, bs, unit_bytes, max_blocks, slots_stride;
+    const char *temp;
+    char *cache;
+    int64_t nb;
+    const int *table, *slots, *n_slots;
+    int *len, *blocks_in_use;
+    unsigned *flags, *status, *counter;
+};
+
+cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, cudaStream_t s);
+cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_commit_kv(const CommitParams &p, int grid, cudaStream_t s);
+int commit_threads();
+size_t commit_smem_bytes(int B);
+
+}  // namespace specv

@@ -1,0 +1,150 @@
+"""The C ABI library builds for sm_103a, loads without a GPU, exports every
+symbol include/spec_verify.h declares, matches the C struct layouts, and
+rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from conftest import ROOT
+from speculative_decoding_verification_37_gb300 import _lib as L
+from speculative_decoding_verification_37_gb300 import build as B
+
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(L.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (spec_\w+)", out.stdout))
+    assert set(names) <= exported
+
+
+def test_build_targets_sm_103a_only():
+    assert B.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_struct_layouts_match_c(lib):
+    src = r"""
+    #include <stdio.h>
+    #include <stddef.h>
+    #include "spec_verify.h"
+    #define P(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
+    int main(void) {
+        printf("SpecChainArgs %zu\nSpecTreeArgs %zu\nSpecCommitArgs %zu\n",
+               sizeof(SpecChainArgs), sizeof(SpecTreeArgs), sizeof(SpecCommitArgs));
+        P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
+        P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
+        P(SpecCommitArgs, flags) P(SpecCommitArgs, num_blocks) P(SpecCommitArgs, slots_stride)
+        return 0;
+    }
+    """
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "l.c")
+        exe = os.path.join(d, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.split() for line in lines if line)
+    structs = {"SpecChainArgs": L.SpecChainArgs, "SpecTreeArgs": L.SpecTreeArgs,
+               "SpecCommitArgs": L.SpecCommitArgs}
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+    for key, val in got.items():
+        if "." in key:
+            s, f = key.split(".")
+            assert getattr(structs[s], f).offset == int(val), key
+
+
+def test_workspace_sizes(lib):
+    assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN, 64, 4, 128256) >= 256 + 64 * 4 + 64 * 5 * 16
+    assert L.spec_workspace_bytes(L.SPEC_WS_TREE, 128, 5, 128256) >= 256 + 128 * 4 + 128 * 5 * 8
+    assert L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 512, 0, 0) >= 512
+    assert L.spec_workspace_bytes(99, 1, 1, 1) == 0
+    assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN, -1, 1, 1) == 0
+
+
+def _chain_args(**over):
+    a = L.SpecChainArgs(B=2, gamma=2, V=16, dtype=L.SPEC_DTYPE_F32, target_logits=4096,
+                        target_row_stride=16, draft_logits=8192, draft_row_stride=16,
+                        draft_tokens=256, uniforms=512, temperature=1.0, top_k=0,
+                        fallback_eps=1e-6, n_acc=1024, out_tokens=2048, n_out=3072,
+                        accept_prob=None, residual_mass=None, flags=None)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(V=0), dict(gamma=-1), dict(B=-1), dict(dtype=7), dict(temperature=-1.0),
+    dict(temperature=float("nan")), dict(top_k=-2), dict(fallback_eps=-1.0),
+    dict(target_logits=None), dict(target_row_stride=15), dict(n_acc=None),
+    dict(draft_tokens=None), dict(uniforms=None), dict(draft_logits=None),
+    dict(draft_row_stride=3), dict(target_logits=4097),
+])
+def test_chain_host_validation(lib, bad):
+    a = _chain_args(**bad)
+    ws = ctypes.create_string_buffer(1 << 16)
+    # host buffers stand in for device pointers: validation must reject first
+    assert lib.spec_verify_chain(ctypes.byref(a), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+
+
+def test_chain_workspace_validation(lib):
+    a = _chain_args()
+    assert lib.spec_verify_chain(ctypes.byref(a), None, 0, None) == L.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_chain(ctypes.byref(a), ctypes.c_void_p(4096), 16, None) == L.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_chain(ctypes.byref(a), ctypes.c_void_p(4097), 1 << 20, None) == L.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_chain(None, None, 0, None) == L.SPEC_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _chain_args(B=0)
+    assert lib.spec_verify_chain(ctypes.byref(a), None, 0, None) == L.SPEC_OK
+    t = L.SpecTreeArgs(B=0, N=3, R=1, V=10, dtype=0)
+    assert lib.spec_verify_tree(ctypes.byref(t), None, 0, None) == L.SPEC_OK
+    c = L.SpecCommitArgs(B=0, L=1, H=1, D=8, S=1, block_size=16, elem_bytes=2, num_blocks=1,
+                         max_blocks=1)
+    assert lib.spec_commit_kv(ctypes.byref(c), None, 0, None) == L.SPEC_OK
+
+
+def test_tree_and_commit_host_validation(lib):
+    ws = ctypes.create_string_buffer(1 << 16)
+    t = L.SpecTreeArgs(B=1, N=2000, R=1, V=10, dtype=0, logits=4096, row_stride=10)
+    assert lib.spec_verify_tree(ctypes.byref(t), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+    t = L.SpecTreeArgs(B=1, N=3, R=0, V=10, dtype=0, logits=4096, row_stride=10)
+    assert lib.spec_verify_tree(ctypes.byref(t), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+    t = L.SpecTreeArgs(B=1, N=3, R=1, V=10, dtype=0, logits=4096, row_stride=10, node_token=256,
+                       node_parent=512, row_of_node=768, path=1024, n_acc=1280, out_tokens=1536,
+                       n_out=1792, pos=2048, committed_len=None)
+    assert lib.spec_verify_tree(ctypes.byref(t), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+    c = L.SpecCommitArgs(B=1, L=1, H=1, D=7, S=1, block_size=16, elem_bytes=2, num_blocks=1,
+                         max_blocks=1, temp_kv=4096, cache=8192, block_table=256, n_slots=512,
+                         committed_len=768)
+    assert lib.spec_commit_kv(ctypes.byref(c), ws, 1 << 16, None) == L.SPEC_ERR_UNSUPPORTED
+    c.D, c.elem_bytes = 8, 3
+    assert lib.spec_commit_kv(ctypes.byref(c), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+    c.elem_bytes, c.cache = 2, 8200
+    assert lib.spec_commit_kv(ctypes.byref(c), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
+
+
+def test_error_strings(lib):
+    assert lib.spec_error_string(L.SPEC_ERR_INVALID_ARG) == b"invalid argument"
+    assert lib.spec_error_string(12345) == b"unknown error code"
