@@ -44,7 +44,9 @@ from typing import List, Optional
 
 import numpy as np
 
-BOUNDARY_MARGIN = 1e-5   # a uniform this close to a decision boundary is a boundary case
+BOUNDARY_MARGIN = 1e-5   # a uniform this close to an acceptance threshold is a boundary case
+DRAW_MARGIN_REL = 3e-11  # a draw whose target u*C_total lies within
+DRAW_MARGIN_ABS = 1e-12  #   REL*C_total + ABS of its token's CDF interval ends is a boundary case
 DEFAULT_EPS = 1e-6       # residual-mass threshold below which the fallback is used
 EPS_BAND = 0.5           # a residual mass within EPS_BAND * eps of eps is a boundary case
 
@@ -115,12 +117,13 @@ class Draw:
     near_boundary: bool
 
 
-def inverse_cdf(weights: np.ndarray, u: float, margin: float = BOUNDARY_MARGIN) -> Draw:
+def inverse_cdf(weights: np.ndarray, u: float, margin_rel: float = DRAW_MARGIN_REL,
+                margin_abs: float = DRAW_MARGIN_ABS) -> Draw:
     """The smallest i with C_i > u * C_total, C_i = sum_{j <= i} w_j in index
     order.  Zero-weight tokens can never be chosen.  If rounding leaves no
     such i, the largest i with w_i > 0 is taken.  ``near_boundary`` is set
-    when u * C_total lies within margin * C_total of either end of the chosen
-    token's CDF interval."""
+    when u * C_total lies within margin_rel * C_total + margin_abs of either
+    end of the chosen token's CDF interval."""
     w = np.asarray(weights, dtype=np.float64)
     C = np.cumsum(w)
     total = C[-1]
@@ -132,7 +135,8 @@ def inverse_cdf(weights: np.ndarray, u: float, margin: float = BOUNDARY_MARGIN) 
         i = int(np.flatnonzero(w > 0)[-1])
     lo = C[i - 1] if i > 0 else 0.0
     hi = C[i]
-    near = (t - lo) < margin * total or (hi - t) < margin * total
+    m = margin_rel * total + margin_abs
+    near = (t - lo) < m or (hi - t) < m
     return Draw(i, bool(near))
 
 
@@ -205,9 +209,9 @@ def verify_chain_sampled(target: np.ndarray, draft: np.ndarray, draft_tokens: np
         if mass <= eps:
             w = P[n_acc]
             res.flags |= FLAG_FALLBACK
-        draw = inverse_cdf(w, u_final, margin)
+        draw = inverse_cdf(w, u_final)
     else:
-        draw = inverse_cdf(P[gamma], u_final, margin)
+        draw = inverse_cdf(P[gamma], u_final)
     res.boundary |= draw.near_boundary
     res.n_acc = n_acc
     res.tokens = d[:n_acc] + [draw.token]
