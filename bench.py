@@ -1,0 +1,470 @@
+"""Benchmark of the batched verify-and-commit step on GB300.
+
+Default workload: chain verification B=64, gamma=4 (5 target rows and 4
+draft rows per request), V=128256, bf16 logits, temperature 0.8, top-k 50,
+followed by the KV commit of every request's accepted prefix into a paged
+bf16 cache (32 layers x 8 KV heads x 128, block 16, 2048-token prefix).  A
+step is one spec_verify_chain + one spec_commit_kv over that batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config {1..5}] [--impl ours|reference]
+
+The metric is target rows verified per second, B*(gamma+1)/t (B*R/t for the
+tree workload), with t the device time of one step; inputs are resident in
+HBM when a step starts and L2 is flushed (a 256 MiB write) between steps.
+`--impl reference` times the fp64 CPU oracle on this machine's cores on a
+bounded sample of the same workload.  Under torchrun every rank runs its own
+batch (weak scaling, no collective on the data path); the slowest rank's
+time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_verification_37_gb300 import workloads as W  # noqa: E402
+
+METRIC = "spec-verify rows/s + achieved HBM GB/s vs peak, B=64 γ=4 V=128256 bf16"
+UNIT = "rows/s"
+L2_FLUSH_BYTES = 256 << 20
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_37_gb300", "csrc")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f.read().splitlines()[1:]:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        smax = max(r[1] for r in rows)
+        loaded = [r[0] for r in rows if r[0] > 0.5 * smax] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workload setup on the device
+# ---------------------------------------------------------------------------
+class Workload:
+    def __init__(self, cfg: int, seed: int, device):
+        self.cfg = cfg
+        self.spec = W.CONFIGS[cfg]
+        self.device = device
+        s = self.spec
+        if isinstance(s, W.TreeSpec):
+            self.kind = "tree"
+            tb = W.make_tree(s, seed=seed)
+            self.host = tb
+            self.rows = s.B * s.n_rows
+            self.logit_bytes = s.logit_bytes()
+            self.kvb = W.make_kv(s.kv, s.B, s.n_nodes + 1, seed=seed)
+        else:
+            self.kind = "chain"
+            cb = W.make_chain(s, seed=seed)
+            self.host = cb
+            self.rows = s.B * (s.gamma + 1)
+            self.logit_bytes = s.logit_bytes()
+            self.kvb = W.make_kv(s.kv, s.B, s.gamma + 1, seed=seed) if s.kv else None
+        self.B = s.B
+        self._to_device()
+
+    def _to_device(self):
+        d = self.device
+        h = self.host
+        if self.kind == "tree":
+            self.inputs = dict(logits=h.logits.to(d), node_token=torch.from_numpy(h.node_token).to(d),
+                               node_parent=torch.from_numpy(h.node_parent).to(d),
+                               row_of_node=torch.from_numpy(h.row_of_node).to(d))
+        else:
+            self.inputs = dict(target=h.target.to(d), draft_tokens=torch.from_numpy(h.draft_tokens).to(d))
+            if h.draft is not None:
+                self.inputs["draft"] = h.draft.to(d)
+                self.inputs["uniforms"] = torch.from_numpy(h.uniforms).to(d)
+        if self.kvb is not None:
+            k = self.kvb
+            self.inputs["temp_kv"] = k.temp_kv.to(d)
+            self.inputs["block_table"] = torch.from_numpy(k.block_table).to(d)
+            self.len0 = torch.from_numpy(k.committed_len.copy()).to(d)
+            self.inputs["committed_len"] = self.len0.clone()
+            self.cache = W.make_cache(k, device=d)
+
+    def host_inputs(self):
+        """Pinned host copies of every per-step input (for the end-to-end run)."""
+        return {k: v.cpu().pin_memory() for k, v in self.inputs.items()}
+
+
+def run_step(wl: Workload, inp, events=None, ws=None):
+    """One verify (+ commit) step; returns the output tensors.  If `events` is
+    given, (start, after_verify, end) are recorded on the current stream."""
+    from speculative_decoding_verification_37_gb300 import api
+    s = wl.spec
+    if events:
+        events[0].record()
+    if wl.kind == "tree":
+        out = api.verify_tree(inp["logits"], inp["node_token"], inp["node_parent"],
+                              inp["row_of_node"], inp["committed_len"], R=s.n_rows)
+        n_slots, slots = out.n_commit, out.commit_slots
+    else:
+        out = api.verify_chain(inp["target"], inp["draft_tokens"], gamma=s.gamma,
+                               temperature=s.temperature, draft=inp.get("draft"),
+                               uniforms=inp.get("uniforms"), top_k=s.top_k, accept_prob=False)
+        n_slots, slots = out.n_out, None
+    if events:
+        events[1].record()
+    if wl.kvb is not None:
+        api.commit_kv(inp["temp_kv"], wl.cache, inp["block_table"], n_slots, inp["committed_len"],
+                      block_size=wl.kvb.kv.block_size, slots=slots)
+    if events:
+        events[2].record()
+    return out
+
+
+def kv_bytes(wl: Workload, n_slots_total: int) -> int:
+    return 0 if wl.kvb is None else 2 * wl.kvb.kv.token_bytes * n_slots_total
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg: int, seconds: float = 12.0, seed: int = 0):
+    """Times the fp64 oracle (verify + commit of each request) on this host,
+    one request at a time, for about `seconds`; returns (rows/s, sample text)."""
+    import oracle as O
+    spec = W.CONFIGS[cfg]
+    rows_done = 0
+    n_req = 0
+    elapsed = 0.0
+    chunk = 4
+    b0 = 0
+    passes = 0
+    while elapsed < seconds:
+        if b0 >= spec.B:          # whole workload done: go round again
+            b0 = 0
+            passes += 1
+        reqs = list(range(b0, min(spec.B, b0 + chunk)))
+        b0 += chunk
+        if isinstance(spec, W.TreeSpec):
+            tb = W.make_tree(spec, seed=seed, requests=reqs)
+            kvb = W.make_kv(spec.kv, len(reqs), spec.n_nodes + 1, seed=seed)
+        else:
+            tb = W.make_chain(spec, seed=seed, requests=reqs)
+            kvb = W.make_kv(spec.kv, len(reqs), spec.gamma + 1, seed=seed) if spec.kv else None
+        if kvb is not None:
+            k = kvb.kv
+            # the commit only reaches each request's tail blocks: a compact cache holds them
+            tails = sorted(set(int(x) for x in kvb.block_table.reshape(-1)) - {0})
+            remap = {blk: i + 1 for i, blk in enumerate(tails)}
+            table = np.vectorize(lambda x: remap.get(int(x), 0))(kvb.block_table).astype(np.int32)
+            cache = np.full((k.layers, 2, len(tails) + 1, k.block_size, k.heads, k.head_dim),
+                            W.KV_SENTINEL, np.int16)
+            temp = kvb.temp_kv.view(torch.int16).numpy()
+        t0 = time.perf_counter()
+        for i in range(len(reqs)):
+            if isinstance(spec, W.TreeSpec):
+                r = O.verify_tree(tb.logits_f64(i), tb.node_token[i], tb.node_parent[i],
+                                  tb.row_of_node[i], int(kvb.committed_len[i]))
+                slots = r.commit_slots
+                rows_done += spec.n_rows
+            elif spec.greedy:
+                r = O.verify_chain_greedy(tb.target_f64(i), tb.draft_tokens[i])
+                slots = O.chain_commit_slots(r.n_acc)
+                rows_done += spec.gamma + 1
+            else:
+                r = O.verify_chain_sampled(tb.target_f64(i), tb.draft_f64(i), tb.draft_tokens[i],
+                                           tb.uniforms[i].astype(np.float64), spec.temperature,
+                                           spec.top_k)
+                slots = O.chain_commit_slots(r.n_acc)
+                rows_done += spec.gamma + 1
+            if kvb is not None:
+                O.commit_kv(cache, temp[i], table[i], slots, len(slots), int(kvb.committed_len[i]),
+                            kvb.kv.block_size)
+            n_req += 1
+        elapsed += time.perf_counter() - t0
+    sample = (f"{n_req} requests ({passes} full passes over the {spec.B} of this workload, then a "
+              f"partial one), verify + KV commit per request, {elapsed:.1f} s of oracle time "
+              f"(input generation excluded)")
+    return rows_done / elapsed, sample, n_req
+
+
+# ---------------------------------------------------------------------------
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def config_dict(cfg: int, world: int):
+    s = W.CONFIGS[cfg]
+    d = {"workload": s.name, "B_per_gpu": s.B, "V": s.V, "dtype": s.dtype,
+         "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+         "parallelism": f"dp{world} (independent request shards, no collective)"}
+    if isinstance(s, W.ChainSpec):
+        d.update(gamma=s.gamma, temperature=s.temperature, top_k=s.top_k)
+    else:
+        d.update(topKSpec=[list(x) for x in s.topKSpec], topHead=list(s.topHead), rows=s.n_rows)
+    if s.kv:
+        d.update(kv=f"{s.kv.layers}L x {s.kv.heads}H x {s.kv.head_dim} bf16, block "
+                    f"{s.kv.block_size}, prefix {s.kv.prefix}")
+    return d
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    v, sample, _ = oracle_sample(args.config, seconds=max(2.0, 4.0 * args.steps))
+    s = W.CONFIGS[args.config]
+    dtype = s.dtype
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": config_dict(args.config, world),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from speculative_decoding_verification_37_gb300 import build as _b
+    _b.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = Workload(args.config, seed=rank, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def reset():
+        if wl.kvb is not None:
+            wl.inputs["committed_len"].copy_(wl.len0)
+
+    # warm-up
+    for _ in range(args.warmup):
+        reset()
+        run_step(wl, wl.inputs)
+    torch.cuda.synchronize()
+
+    # timed steps: per-step events; the reset and the L2 flush sit between events
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    n_commit_total = 0
+    outs = []
+    for i in range(args.steps):
+        reset()
+        flush.zero_()
+        outs.append(run_step(wl, wl.inputs, events=ev[i]))
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    verify_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    commit_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if wl.kvb is not None:
+        o = outs[-1]
+        n_commit_total = int((o.n_commit if wl.kind == "tree" else o.n_out).sum().item())
+    t_step = statistics.mean(step_ms)
+    t_step_max = max_over_ranks(t_step, world)
+    rows_total = wl.rows * world
+    value = rows_total / (t_step_max * 1e-3)
+
+    peak, peak_kind = measured_peaks()
+    t_verify = statistics.mean(verify_ms)
+    achieved = wl.logit_bytes / (t_verify * 1e-3) / 1e9
+    kname = "argmax_verify_kernel" if (wl.kind == "tree" or wl.spec.greedy) else "chain_sample_kernel"
+    tr = traffic_record(kname)
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None if tr is None else tr["bytes_per_launch"],
+                "algorithmic_bytes": wl.logit_bytes, "avg_launch_ms": round(t_verify, 5),
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
+    commit = None
+    if wl.kvb is not None:
+        t_commit = statistics.mean(commit_ms)
+        kvb = kv_bytes(wl, n_commit_total)
+        commit = {"kernel": "commit_kv_kernel", "avg_launch_ms": round(t_commit, 5),
+                  "algorithmic_bytes": kvb, "achieved_gbs": round(kvb / (t_commit * 1e-3) / 1e9, 1),
+                  "frac": round(kvb / (t_commit * 1e-3) / 1e9 / peak, 4),
+                  "committed_tokens": n_commit_total}
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hin = wl.host_inputs()
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d_in = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+        e_steps = max(3, min(args.steps, 10))
+        times = []
+        d2h = 0
+        for i in range(e_steps + 2):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for k, v in hin.items():
+                d_in[k].copy_(v, non_blocking=True)
+            o = run_step(wl, d_in)
+            res = [o.n_acc, o.out_tokens, o.n_out] + ([d_in["committed_len"]] if wl.kvb else [])
+            host = [r.to("cpu", non_blocking=True) for r in res]
+            t1.record()
+            torch.cuda.synchronize()
+            d2h = sum(r.numel() * r.element_size() for r in host)
+            if i >= 2:
+                times.append(t0.elapsed_time(t1))
+        t_e2e = max_over_ranks(statistics.mean(times), world)
+        e2e = {"value": rows_total / (t_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e, 4),
+               "path": "pinned host -> device copies, spec_verify + spec_commit_kv, device -> host "
+                       "of n_acc/out_tokens/n_out/committed_len, all in the timed region"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, _ = oracle_sample(args.config, seconds=12.0)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_max, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": W.CONFIGS[args.config].dtype, "data": "synthetic",
+                "config": config_dict(args.config, world),
+                "rounds_per_s": wl.B * world / (t_step_max * 1e-3),
+                "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /
+                                  (t_step_max * 1e-3) / 1e9, 1),
+                "roofline": roofline, "commit": commit, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * (2 if wl.kvb is not None else 1),
+                "clocks": clk, "kernel_source": kernel_source_hash()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

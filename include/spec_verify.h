@@ -200,7 +200,7 @@ typedef struct SpecCommitArgs {
     const int32_t *block_table;  /* device, int32 [B][max_blocks] */
     int32_t max_blocks;
     const int32_t *slots;        /* device, int32 [B][slots_stride] or NULL (identity) */
-    int32_t slots_stride;
+    int32_t slots_stride;        /* >= S when slots != NULL */
     const int32_t *n_slots;      /* device, int32 [B] */
     int32_t *committed_len;      /* device, int32 [B], in/out */
     int32_t *blocks_in_use;      /* device out [B] or NULL */

@@ -46,17 +46,38 @@ int slice_len(int V, int c) {
 
 struct Ws {
     unsigned *status;
-    unsigned *counters;
+    unsigned *counters;  // [B] arrival counters
+    unsigned *rejword;   // [B] earliest rejection per request (chain, sampled)
     void *data;
 };
 
 Ws ws_layout(void *ws, int B) {
     char *base = static_cast<char *>(ws);
+    const size_t per_req = ws_align((size_t)B * sizeof(unsigned));
     Ws w;
     w.status = reinterpret_cast<unsigned *>(base);
     w.counters = reinterpret_cast<unsigned *>(base + kWsHeader);
-    w.data = base + kWsHeader + ws_align((size_t)B * sizeof(unsigned));
+    w.rejword = reinterpret_cast<unsigned *>(base + kWsHeader + per_req);
+    w.data = base + kWsHeader + 2 * per_req;
     return w;
+}
+
+// Double-float constants for the on-device exp2: ln 2 and 2^(j/64), j = -32..32,
+// each value computed in double on the host and split as hi = (float)v,
+// lo = (float)(v - hi).
+void split(double v, float2 &out) {
+    out.x = (float)v;
+    out.y = (float)(v - (double)out.x);
+}
+
+const DdExpTables &exp_tables() {
+    static const DdExpTables t = [] {
+        DdExpTables x;
+        split(0.69314718055994530942, x.ln2);
+        for (int j = -32; j <= 32; ++j) split(std::exp2((double)j / 64.0), x.tab[j + 32]);
+        return x;
+    }();
+    return t;
 }
 
 }  // namespace
@@ -64,7 +85,7 @@ Ws ws_layout(void *ws, int B) {
 extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V) {
     (void)V;
     if (B < 0 || n < 0) return 0;
-    const size_t head = kWsHeader + ws_align((size_t)B * sizeof(unsigned));
+    const size_t head = kWsHeader + 2 * ws_align((size_t)B * sizeof(unsigned));
     switch (kind) {
     case SPEC_WS_CHAIN: {
         const size_t rows = (size_t)B * ((size_t)n + 1);
@@ -141,7 +162,13 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.dstride = a->draft_row_stride;
         p.tokens = a->draft_tokens;
         p.unif = a->uniforms;
-        p.c2 = (float)(1.4426950408889634 / (double)a->temperature);
+        const double c2 = 1.4426950408889634074 / (double)a->temperature;
+        p.c2 = (float)c2;
+        float2 c2s;
+        split(c2, c2s);
+        p.c2_hi = c2s.x;
+        p.c2_lo = c2s.y;
+        p.exptab = exp_tables();
         p.top_k = (a->top_k >= a->V) ? 0 : a->top_k;
         p.eps = a->fallback_eps;
         p.n_acc = a->n_acc;
@@ -152,6 +179,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.flags = a->flags;
         p.status = w.status;
         p.counters = w.counters;
+        p.rejword = w.rejword;
         p.recs = static_cast<PosRec *>(w.data);
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
         if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
@@ -219,7 +247,7 @@ extern "C" int spec_commit_kv(const SpecCommitArgs *a, void *workspace, size_t w
     if (!a->temp_kv || !a->cache || !a->block_table || !a->n_slots || !a->committed_len)
         return SPEC_ERR_INVALID_ARG;
     if (!aligned(a->temp_kv, 16) || !aligned(a->cache, 16)) return SPEC_ERR_INVALID_ARG;
-    if (a->slots && a->slots_stride < 1) return SPEC_ERR_INVALID_ARG;
+    if (a->slots && a->slots_stride < a->S) return SPEC_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || ws_bytes < spec_workspace_bytes(SPEC_WS_COMMIT, a->B, 0, 0))
         return SPEC_ERR_INVALID_ARG;
     char *base = static_cast<char *>(workspace);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ddmath.cuh"
+
 namespace specv {
 
 // Workspace layout shared by every verify kind: a sticky status word, one
@@ -41,6 +43,8 @@ struct ArgmaxParams {
     unsigned *flags;
 };
 
+constexpr int kTopKFastMax = 128;  // top_k served by the candidate-list path
+
 struct SampleParams {
     int B, gamma, V, c, Vs;
     const void *target;
@@ -50,12 +54,15 @@ struct SampleParams {
     const int *tokens;
     const float *unif;
     float c2;      // log2(e) / temperature
+    float c2_hi, c2_lo;   // the same as a double-float pair
+    DdExpTables exptab;   // ln 2 and 2^(j/64) as double-float pairs
     int top_k;     // 0 = keep all
     float eps;
     int *n_acc, *out_tokens, *n_out;
     float *accept_prob, *resid;
     unsigned *flags;
     unsigned *status, *counters;
+    unsigned *rejword;  // [B] earliest rejection seen: gamma - k + 1, 0 = none
     PosRec *recs;  // [B*(gamma+1)]
 };
 
