@@ -58,6 +58,7 @@ extern "C" {
 #define SPEC_ERR_INVALID_ARG 1
 #define SPEC_ERR_UNSUPPORTED 2
 #define SPEC_ERR_CUDA 3
+#define SPEC_ERR_TOO_LARGE 4 /* spec_verify_chain_static: the call needs more than its fixed scratch */
 
 /* logits element types */
 #define SPEC_DTYPE_BF16 0
@@ -209,6 +210,40 @@ typedef struct SpecCommitArgs {
 
 int spec_commit_kv(const SpecCommitArgs *args, void *workspace, size_t workspace_bytes,
                    void *stream);
+
+/*
+ * spec_verify_chain_static — spec_verify_chain for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this is a
+ * deployment variant of the same computation.
+ *
+ * Some callers cannot call cudaMalloc where they verify a round: code
+ * running under a memory-pool or arena allocator that owns every device
+ * byte, plug-ins whose host framework forbids allocation on its hot path,
+ * and callers that must avoid an allocation's implicit synchronisation.
+ * This call takes the same arguments as spec_verify_chain minus the
+ * workspace: its scratch (arrival counters, rejection words, per-position
+ * records) is a fixed array of SPEC_STATIC_WORKSPACE_BYTES compiled into the
+ * library, resident on every GPU that loads it until the process exits.
+ *
+ *   * Inputs and outputs are still the caller's device buffers, exactly as
+ *     for spec_verify_chain, and the results are identical to it.
+ *   * It allocates nothing (no cudaMalloc, cudaFree or allocating library
+ *     routine).  It enqueues one small memset of the zero-initialised part
+ *     of the array, then the verify kernel, on `stream`.
+ *   * The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   * All calls on one GPU share the array and it keeps the last call's
+ *     contents: calls whose kernels could overlap on the GPU race on it, so
+ *     order them on one stream.
+ *   * A call needing more scratch than the array holds (see
+ *     spec_workspace_bytes(SPEC_WS_CHAIN, B, gamma, V)) returns
+ *     SPEC_ERR_TOO_LARGE before enqueuing anything.  1 MiB covers, e.g.,
+ *     B = 4096 requests at gamma = 8.
+ *   * There is no status word to read back: data errors show in flags[b].
+ */
+#define SPEC_STATIC_WORKSPACE_BYTES (1u << 20)
+int spec_verify_chain_static(const SpecChainArgs *args, void *stream);
 
 /* Workspace bytes for a call of the given kind (n = gamma for SPEC_WS_CHAIN,
  * R for SPEC_WS_TREE, ignored for SPEC_WS_COMMIT).  Returns 0 for an unknown

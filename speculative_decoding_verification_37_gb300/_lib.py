@@ -16,13 +16,15 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
 
-SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
+SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_TOO_LARGE = 0, 1, 2, 3, 4
+SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
 SPEC_DTYPE_BF16, SPEC_DTYPE_F32 = 0, 1
 SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW = 1, 2, 4
 SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT = 0, 1, 2
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
-            "spec_get_status", "spec_error_string", "spec_last_cuda_error")
+            "spec_get_status", "spec_error_string", "spec_last_cuda_error",
+            "spec_verify_chain_static")
 
 
 class SpecChainArgs(ctypes.Structure):
@@ -86,6 +88,8 @@ def lib():
         L.spec_get_status.restype = c_int
         L.spec_error_string.argtypes = [c_int]
         L.spec_error_string.restype = c_char_p
+        L.spec_verify_chain_static.argtypes = [POINTER(SpecChainArgs), c_void_p]
+        L.spec_verify_chain_static.restype = c_int
         L.spec_last_cuda_error.argtypes = []
         L.spec_last_cuda_error.restype = c_char_p
         _LIB = L
@@ -195,3 +199,29 @@ def spec_commit_kv(*, temp_kv: torch.Tensor, cache: torch.Tensor, block_table: t
                        blocks_in_use=_ptr(blocks_in_use), flags=_ptr(flags))
     _check("spec_commit_kv", lib().spec_commit_kv(
         ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                             n_acc: torch.Tensor, out_tokens: torch.Tensor, n_out: torch.Tensor,
+                             gamma: int, temperature: float,
+                             draft_logits: Optional[torch.Tensor] = None,
+                             uniforms: Optional[torch.Tensor] = None, top_k: int = 0,
+                             fallback_eps: float = 1e-6, accept_prob: Optional[torch.Tensor] = None,
+                             residual_mass: Optional[torch.Tensor] = None,
+                             flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Marshals one spec_verify_chain_static call: the same as
+    spec_verify_chain, but the library's fixed device array is the scratch,
+    for callers that cannot allocate device memory."""
+    V = target_logits.shape[-1]
+    B = target_logits.shape[0] // (gamma + 1)
+    a = SpecChainArgs(B=B, gamma=gamma, V=V, dtype=_dtype_code(target_logits),
+                      target_logits=_ptr(target_logits), target_row_stride=target_logits.stride(0),
+                      draft_logits=_ptr(draft_logits),
+                      draft_row_stride=draft_logits.stride(0) if draft_logits is not None else 0,
+                      draft_tokens=_ptr(draft_tokens), uniforms=_ptr(uniforms),
+                      temperature=float(temperature), top_k=int(top_k),
+                      fallback_eps=float(fallback_eps), n_acc=_ptr(n_acc),
+                      out_tokens=_ptr(out_tokens), n_out=_ptr(n_out),
+                      accept_prob=_ptr(accept_prob), residual_mass=_ptr(residual_mass),
+                      flags=_ptr(flags))
+    _check("spec_verify_chain_static", lib().spec_verify_chain_static(ctypes.byref(a), _stream(stream)))

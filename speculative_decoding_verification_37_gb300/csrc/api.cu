@@ -296,6 +296,7 @@ extern "C" const char *spec_error_string(int code) {
     case SPEC_ERR_INVALID_ARG: return "invalid argument";
     case SPEC_ERR_UNSUPPORTED: return "unsupported configuration";
     case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_TOO_LARGE: return "request needs more scratch than the static workspace holds";
     default: return "unknown error code";
     }
 }
