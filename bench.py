@@ -129,9 +129,10 @@ class ClockSampler:
 # workload setup on the device
 # ---------------------------------------------------------------------------
 class Workload:
-    def __init__(self, cfg: int, seed: int, device):
+    def __init__(self, cfg: int, seed: int, device, batch=None):
+        import dataclasses
         self.cfg = cfg
-        self.spec = W.CONFIGS[cfg]
+        self.spec = W.CONFIGS[cfg] if not batch else dataclasses.replace(W.CONFIGS[cfg], B=batch)
         self.device = device
         s = self.spec
         if isinstance(s, W.TreeSpec):
@@ -177,12 +178,10 @@ class Workload:
 
 
 def run_step(wl: Workload, inp, events=None, ws=None):
-    """One verify (+ commit) step; returns the output tensors.  If `events` is
-    given, (start, after_verify, end) are recorded on the current stream."""
+    """One verify (+ commit) step through the public API (allocates its
+    outputs); used for the end-to-end measurement.  Returns the outputs."""
     from speculative_decoding_verification_37_gb300 import api
     s = wl.spec
-    if events:
-        events[0].record()
     if wl.kind == "tree":
         out = api.verify_tree(inp["logits"], inp["node_token"], inp["node_parent"],
                               inp["row_of_node"], inp["committed_len"], R=s.n_rows)
@@ -192,14 +191,102 @@ def run_step(wl: Workload, inp, events=None, ws=None):
                                temperature=s.temperature, draft=inp.get("draft"),
                                uniforms=inp.get("uniforms"), top_k=s.top_k, accept_prob=False)
         n_slots, slots = out.n_out, None
-    if events:
-        events[1].record()
     if wl.kvb is not None:
         api.commit_kv(inp["temp_kv"], wl.cache, inp["block_table"], n_slots, inp["committed_len"],
                       block_size=wl.kvb.kv.block_size, slots=slots)
-    if events:
-        events[2].record()
     return out
+
+
+class Step:
+    """The timed step with every output and workspace preallocated, the
+    verify call and the commit call each captured in a CUDA graph so that
+    the timed region holds GPU work only (no allocation, no host latency)."""
+
+    def __init__(self, wl: Workload):
+        from speculative_decoding_verification_37_gb300 import _lib as L
+        self.wl = wl
+        s, dev, inp = wl.spec, wl.device, wl.inputs
+        i32 = dict(dtype=torch.int32, device=dev)
+        B = wl.B
+        if wl.kind == "tree":
+            N, R = s.n_nodes, s.n_rows
+            W_ = (N + 1 + 31) // 32
+            self.out = dict(path=torch.empty((B, N), **i32), n_acc=torch.empty(B, **i32),
+                            out_tokens=torch.empty((B, N + 1), **i32), n_out=torch.empty(B, **i32),
+                            tree_mask=torch.empty((B, N + 1, W_), **i32),
+                            pos=torch.empty((B, N + 1), **i32), commit_slots=torch.empty((B, N + 1), **i32),
+                            n_commit=torch.empty(B, **i32), flags=torch.empty(B, **i32))
+            self.ws = L.new_workspace(L.SPEC_WS_TREE, B, R, s.V, dev)
+
+            def verify():
+                L.spec_verify_tree(logits=inp["logits"], R=R, node_token=inp["node_token"],
+                                   node_parent=inp["node_parent"], row_of_node=inp["row_of_node"],
+                                   committed_len=inp["committed_len"], workspace=self.ws, **self.out)
+            self.n_slots, self.slots = self.out["n_commit"], self.out["commit_slots"]
+        else:
+            g = s.gamma
+            self.out = dict(n_acc=torch.empty(B, **i32), out_tokens=torch.empty((B, g + 1), **i32),
+                            n_out=torch.empty(B, **i32), flags=torch.empty(B, **i32))
+            kind = L.SPEC_WS_CHAIN_TOPK if (not s.greedy and 0 < s.top_k <= L.TOPK_FAST_MAX) else L.SPEC_WS_CHAIN
+            self.ws = L.new_workspace(kind, B, g, s.V, dev)
+
+            def verify():
+                L.spec_verify_chain(target_logits=inp["target"], draft_tokens=inp["draft_tokens"],
+                                    workspace=self.ws, gamma=g, temperature=s.temperature,
+                                    draft_logits=inp.get("draft"), uniforms=inp.get("uniforms"),
+                                    top_k=s.top_k, **self.out)
+            self.n_slots, self.slots = self.out["n_out"], None
+        self.verify = verify
+        self.commit = None
+        if wl.kvb is not None:
+            self.cws = L.new_workspace(L.SPEC_WS_COMMIT, B, 0, 0, dev)
+
+            def commit():
+                L.spec_commit_kv(temp_kv=inp["temp_kv"], cache=wl.cache, block_table=inp["block_table"],
+                                 n_slots=self.n_slots, committed_len=inp["committed_len"],
+                                 block_size=wl.kvb.kv.block_size, workspace=self.cws, slots=self.slots)
+            self.commit = commit
+        self.graphs = None
+
+    def reset(self):
+        if self.wl.kvb is not None:
+            self.wl.inputs["committed_len"].copy_(self.wl.len0)
+
+    def eager(self):
+        self.reset()
+        self.verify()
+        if self.commit:
+            self.commit()
+
+    def capture(self):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                self.eager()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.gv = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.gv):
+            self.verify()
+        self.gc = None
+        if self.commit:
+            self.reset()
+            self.gc = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.gc):
+                self.commit()
+        torch.cuda.synchronize()
+
+    def replay(self, events=None):
+        if events:
+            events[0].record()
+        self.gv.replay()
+        if events:
+            events[1].record()
+        if self.gc is not None:
+            self.gc.replay()
+        if events:
+            events[2].record()
 
 
 def kv_bytes(wl: Workload, n_slots_total: int) -> int:
@@ -300,8 +387,9 @@ def barrier(world: int):
         dist.barrier()
 
 
-def config_dict(cfg: int, world: int):
-    s = W.CONFIGS[cfg]
+def config_dict(cfg: int, world: int, batch: int = 0):
+    import dataclasses
+    s = W.CONFIGS[cfg] if not batch else dataclasses.replace(W.CONFIGS[cfg], B=batch)
     d = {"workload": s.name, "B_per_gpu": s.B, "V": s.V, "dtype": s.dtype,
          "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
          "parallelism": f"dp{world} (independent request shards, no collective)"}
@@ -340,6 +428,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's request count (smaller cases for profiling)")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     if args.impl == "reference":
@@ -352,41 +442,36 @@ def main():
     _b.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = Workload(args.config, seed=rank, device=dev)
+    wl = Workload(args.config, seed=rank, device=dev, batch=args.batch)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def reset():
-        if wl.kvb is not None:
-            wl.inputs["committed_len"].copy_(wl.len0)
+    step = Step(wl)
+    step.capture()
 
     # warm-up
     for _ in range(args.warmup):
-        reset()
-        run_step(wl, wl.inputs)
+        step.reset()
+        step.replay()
     torch.cuda.synchronize()
 
-    # timed steps: per-step events; the reset and the L2 flush sit between events
+    # timed steps: per-step events around the graph replays; the length reset
+    # and the L2 flush (which also keeps the GPU busy while the host enqueues)
+    # sit between the events
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    n_commit_total = 0
-    outs = []
     for i in range(args.steps):
-        reset()
+        step.reset()
         flush.zero_()
-        outs.append(run_step(wl, wl.inputs, events=ev[i]))
+        step.replay(events=ev[i])
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     verify_ms = [e[0].elapsed_time(e[1]) for e in ev]
     commit_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    if wl.kvb is not None:
-        o = outs[-1]
-        n_commit_total = int((o.n_commit if wl.kind == "tree" else o.n_out).sum().item())
+    n_commit_total = int(step.n_slots.sum().item()) if wl.kvb is not None else 0
     t_step = statistics.mean(step_ms)
     t_step_max = max_over_ranks(t_step, world)
     rows_total = wl.rows * world
@@ -453,7 +538,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_max, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": W.CONFIGS[args.config].dtype, "data": "synthetic",
-                "config": config_dict(args.config, world),
+                "config": config_dict(args.config, world, args.batch),
                 "rounds_per_s": wl.B * world / (t_step_max * 1e-3),
                 "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /
                                   (t_step_max * 1e-3) / 1e9, 1),

@@ -68,11 +68,15 @@ extern "C" {
 #define SPEC_FLAG_BAD_INPUT 1u  /* token / node / slot / block id out of range: request skipped */
 #define SPEC_FLAG_FALLBACK 2u   /* residual mass <= fallback_eps: the draw used p_k itself */
 #define SPEC_FLAG_BAD_ROW 4u    /* every kept logit of a row is -inf: request skipped */
+#define SPEC_FLAG_TIMEOUT 8u    /* a bulk copy did not complete within its wait limit (status word
+                                   only): outputs of the call are not valid */
 
 /* workspace kinds for spec_workspace_bytes */
 #define SPEC_WS_CHAIN 0 /* n = gamma */
 #define SPEC_WS_TREE 1  /* n = R (logits rows per request) */
 #define SPEC_WS_COMMIT 2
+#define SPEC_WS_CHAIN_TOPK 3 /* n = gamma: SPEC_WS_CHAIN plus the candidate pool (32 KiB per
+                                request position) of the fast top-k path (0 < top_k <= 128) */
 
 /*
  * Chain verification, sampled (temperature > 0) or greedy (temperature == 0).
@@ -101,8 +105,14 @@ extern "C" {
  *   accepted drafts then the drawn token (row stride gamma+1); n_out[b] =
  *   n_acc[b] + 1.  Optional (NULL = not written): accept_prob[b][k] = a_k for
  *   every k (sampled only); residual_mass[b][k] = sum max(0, p_k - q_k) for
- *   every k (sampled only; costs a second on-chip pass over every row pair);
- *   flags[b].
+ *   every k (sampled only; costs a second pass, served from L2, over every
+ *   row pair); flags[b].
+ * Workspace: spec_workspace_bytes(SPEC_WS_CHAIN, B, gamma, V) bytes suffice
+ *   for every call.  Sampled calls with 0 < top_k <= 128 take a faster path
+ *   (cluster-free candidate lists) when the workspace holds
+ *   spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, B, gamma, V) bytes; with less
+ *   they take the exact cluster-wide threshold search instead.  Both give
+ *   identical results.
  */
 typedef struct SpecChainArgs {
     int32_t B, gamma, V, dtype;

@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecveri
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_TOO_LARGE = 0, 1, 2, 3, 4
 SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
 SPEC_DTYPE_BF16, SPEC_DTYPE_F32 = 0, 1
-SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW = 1, 2, 4
-SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT = 0, 1, 2
+SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW, SPEC_FLAG_TIMEOUT = 1, 2, 4, 8
+SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT, SPEC_WS_CHAIN_TOPK = 0, 1, 2, 3
+TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspace holds it
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
             "spec_get_status", "spec_error_string", "spec_last_cuda_error",

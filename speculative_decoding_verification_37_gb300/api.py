@@ -57,7 +57,8 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
         if (sampled and residual_mass) else None,
         flags=torch.zeros(B, dtype=torch.int32, device=dev))
     if ws is None:
-        ws = workspace(L.SPEC_WS_CHAIN, B, gamma, V, dev)
+        kind = L.SPEC_WS_CHAIN_TOPK if (sampled and 0 < top_k <= L.TOPK_FAST_MAX) else L.SPEC_WS_CHAIN
+        ws = workspace(kind, B, gamma, V, dev)
     L.spec_verify_chain(target_logits=target, draft_tokens=draft_tokens, n_acc=out.n_acc,
                         out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws, gamma=gamma,
                         temperature=temperature, draft_logits=draft, uniforms=uniforms,

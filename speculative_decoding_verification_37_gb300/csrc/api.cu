@@ -1,6 +1,7 @@
 // C ABI of the verify-and-commit library: argument validation, workspace
 // layout, launch configuration.  No allocation, no synchronisation (except
 // spec_get_status, which says so), no stream creation.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -24,17 +25,22 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t esize(int dtype) { return dtype == SPEC_DTYPE_BF16 ? 2 : 4; }
 
 int sm_count() {
+    static std::atomic<int> cached[64];
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-    return n > 0 ? n : 148;
+    if (dev >= 0 && dev < 64 && cached[dev].load() > 0) return cached[dev].load();
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev >= 0 && dev < 64) cached[dev].store(n);
+    return n;
 }
 
-// Slices per row: about 64 KiB of logits per block, at most 8 (cluster limit).
-int slices_for(int V, int dtype, int max_slices) {
-    const int64_t bytes = (int64_t)V * (int64_t)esize(dtype);
-    int64_t c = (bytes + 65535) / 65536;
+// Slices per row: the fewest (at most max_slices) whose 16-byte-rounded length
+// keeps one slice within `limit` bytes.
+int slices_for(int V, int dtype, int max_slices, int64_t limit = 65536) {
+    const int64_t e = (int64_t)esize(dtype);
+    int64_t c = ((int64_t)V * e + limit - 1) / limit;
     if (c < 1) c = 1;
+    while (c < max_slices && ((((int64_t)V + c - 1) / c + 7) & ~int64_t(7)) * e > limit) ++c;
     if (c > max_slices) c = max_slices;
     return (int)c;
 }
@@ -48,18 +54,43 @@ struct Ws {
     unsigned *status;
     unsigned *counters;  // [B] arrival counters
     unsigned *rejword;   // [B] earliest rejection per request (chain, sampled)
-    void *data;
+    void *data;          // chain: records or argmax keys; tree: argmax keys
+    unsigned *poscnt;    // chain: [B*(gamma+1)] top-k arrivals per position
+    unsigned *poolcnt;   // chain: [B*(gamma+1)][2]
+    uint2 *pool;         // chain: [B*(gamma+1)][2][kTopKPool]
 };
 
-Ws ws_layout(void *ws, int B) {
-    char *base = static_cast<char *>(ws);
+// One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
+// (0 for other kinds), `data_bytes` the per-row keys or records.
+size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_ptr, bool with_pool) {
+    char *base = static_cast<char *>(base_ptr);
+    size_t off = kWsHeader;
     const size_t per_req = ws_align((size_t)B * sizeof(unsigned));
-    Ws w;
-    w.status = reinterpret_cast<unsigned *>(base);
-    w.counters = reinterpret_cast<unsigned *>(base + kWsHeader);
-    w.rejword = reinterpret_cast<unsigned *>(base + kWsHeader + per_req);
-    w.data = base + kWsHeader + 2 * per_req;
-    return w;
+    if (w) {
+        w->status = reinterpret_cast<unsigned *>(base);
+        w->counters = reinterpret_cast<unsigned *>(base + off);
+        w->rejword = reinterpret_cast<unsigned *>(base + off + per_req);
+    }
+    off += 2 * per_req;
+    if (w) w->data = base + off;
+    off += ws_align(data_bytes);
+    if (!with_pool) {
+        if (w) w->poscnt = w->poolcnt = nullptr, w->pool = nullptr;
+        return off;
+    }
+    if (w) w->poscnt = reinterpret_cast<unsigned *>(base + off);
+    off += ws_align(rows * sizeof(unsigned));
+    if (w) w->poolcnt = reinterpret_cast<unsigned *>(base + off);
+    off += ws_align(rows * 2 * sizeof(unsigned));
+    if (w) w->pool = reinterpret_cast<uint2 *>(base + off);
+    off += ws_align(rows * 2 * (size_t)kTopKPool * sizeof(uint2));
+    return off;
+}
+
+size_t chain_data_bytes(size_t rows) {
+    const size_t rec = rows * sizeof(PosRec);
+    const size_t keys = rows * sizeof(unsigned long long);
+    return rec > keys ? rec : keys;
 }
 
 // Double-float constants for the on-device exp2: ln 2 and 2^(j/64), j = -32..32,
@@ -85,16 +116,15 @@ const DdExpTables &exp_tables() {
 extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V) {
     (void)V;
     if (B < 0 || n < 0) return 0;
-    const size_t head = kWsHeader + 2 * ws_align((size_t)B * sizeof(unsigned));
     switch (kind) {
-    case SPEC_WS_CHAIN: {
+    case SPEC_WS_CHAIN:
+    case SPEC_WS_CHAIN_TOPK: {
         const size_t rows = (size_t)B * ((size_t)n + 1);
-        const size_t rec = rows * sizeof(PosRec);
-        const size_t keys = rows * sizeof(unsigned long long);
-        return head + ws_align(rec > keys ? rec : keys);
+        return ws_layout_bytes(B, rows, chain_data_bytes(rows), nullptr, nullptr, kind == SPEC_WS_CHAIN_TOPK);
     }
     case SPEC_WS_TREE:
-        return head + ws_align((size_t)B * (size_t)n * sizeof(unsigned long long));
+        return ws_layout_bytes(B, 0, (size_t)B * (size_t)n * sizeof(unsigned long long), nullptr, nullptr,
+                               false);
     case SPEC_WS_COMMIT:
         return 2 * kWsHeader;
     default:
@@ -126,7 +156,9 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     if (!workspace || !aligned(workspace, 256) ||
         ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
         return SPEC_ERR_INVALID_ARG;
-    const Ws w = ws_layout(workspace, a->B);
+    const bool has_pool = ws_bytes >= spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, a->B, a->gamma, a->V);
+    Ws w;
+    ws_layout_bytes(a->B, (size_t)rows, chain_data_bytes((size_t)rows), &w, workspace, has_pool);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (greedy) {
@@ -134,7 +166,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.rows = a->target_logits;
         p.stride = a->target_row_stride;
         p.V = a->V;
-        p.slices = slices_for(a->V, a->dtype, 64);
+        p.slices = slices_for(a->V, a->dtype, 1 << 20);
         p.slice_len = slice_len(a->V, p.slices);
         p.rows_per_req = a->gamma + 1;
         p.keys = static_cast<unsigned long long *>(w.data);
@@ -154,7 +186,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.B = a->B;
         p.gamma = a->gamma;
         p.V = a->V;
-        p.c = slices_for(a->V, a->dtype, 8);
+        p.c = slices_for(a->V, a->dtype, 8, 32768);
         p.Vs = slice_len(a->V, p.c);
         p.target = a->target_logits;
         p.tstride = a->target_row_stride;
@@ -181,9 +213,25 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.counters = w.counters;
         p.rejword = w.rejword;
         p.recs = static_cast<PosRec *>(w.data);
+        p.poscnt = w.poscnt;
+        p.poolcnt = w.poolcnt;
+        p.pool = w.pool;
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
-        if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
-        e = launch_chain_sample(p, a->dtype, s);
+        // top-k <= 128: cluster-free candidate lists when every slice's share
+        // (about k + a few) fits the per-position pool; otherwise the cluster
+        // kernel with its exact threshold search
+        const int cf = slices_for(a->V, a->dtype, 1 << 20, 32768);
+        const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax &&
+                          (int64_t)cf * (p.top_k + 16) <= kTopKPool;
+        if (fast) {
+            p.c = cf;
+            p.Vs = slice_len(a->V, cf);
+            if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+            e = launch_chain_topk(p, a->dtype, s);
+        } else {
+            if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+            e = launch_chain_sample(p, a->dtype, s);
+        }
     }
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
@@ -203,12 +251,13 @@ extern "C" int spec_verify_tree(const SpecTreeArgs *a, void *workspace, size_t w
         ws_bytes < spec_workspace_bytes(SPEC_WS_TREE, a->B, a->R, a->V))
         return SPEC_ERR_INVALID_ARG;
     const int64_t rows = (int64_t)a->B * a->R;
-    const Ws w = ws_layout(workspace, a->B);
+    Ws w;
+    ws_layout_bytes(a->B, 0, (size_t)rows * sizeof(unsigned long long), &w, workspace, false);
     ArgmaxParams p = {};
     p.rows = a->logits;
     p.stride = a->row_stride;
     p.V = a->V;
-    p.slices = slices_for(a->V, a->dtype, 64);
+    p.slices = slices_for(a->V, a->dtype, 1 << 20);
     p.slice_len = slice_len(a->V, p.slices);
     p.rows_per_req = a->R;
     p.keys = static_cast<unsigned long long *>(w.data);

@@ -145,8 +145,9 @@ __global__ void __launch_bounds__(kCommitNT) commit_kv_kernel(CommitParams p) {
 cudaError_t launch_commit_kv(const CommitParams &p, int grid, cudaStream_t s) {
     const size_t smem = commit_smem_bytes(p.B);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(commit_kv_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // the largest B (32768) needs the most; set that once per device
+        static std::atomic<unsigned long long> done{0};
+        cudaError_t e = ensure_smem_attr(commit_kv_kernel, (int)commit_smem_bytes(32768), done);
         if (e != cudaSuccess) return e;
     }
     commit_kv_kernel<<<grid, kCommitNT, smem, s>>>(p);

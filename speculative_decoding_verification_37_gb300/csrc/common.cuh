@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "spec_verify.h"
 
 namespace specv {
@@ -243,6 +245,20 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 }
 __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
     return (int)(~(uint32_t)(k & 0xffffffffull));
+}
+
+// Sets a kernel's dynamic shared-memory limit once per device (the setting
+// is per device; doing it once keeps it out of captured launch sequences).
+template <typename K>
+inline cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<unsigned long long> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 }  // namespace specv

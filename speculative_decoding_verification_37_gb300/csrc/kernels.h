@@ -63,8 +63,13 @@ struct SampleParams {
     unsigned *flags;
     unsigned *status, *counters;
     unsigned *rejword;  // [B] earliest rejection seen: gamma - k + 1, 0 = none
-    PosRec *recs;  // [B*(gamma+1)]
+    PosRec *recs;       // [B*(gamma+1)]
+    unsigned *poscnt;   // [B*(gamma+1)] top-k path: slices arrived per position
+    unsigned *poolcnt;  // [B*(gamma+1)][2] top-k path: candidates appended per row
+    uint2 *pool;        // [B*(gamma+1)][2][kTopKPool] top-k path: candidate (key, token)
 };
+
+constexpr int kTopKPool = 2048;   // candidate entries per row per position (top-k path)
 
 struct CommitParams {
     int B, L, S, bs, unit_bytes, max_blocks, slots_stride;
@@ -78,6 +83,7 @@ struct CommitParams {
 
 cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, cudaStream_t s);
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_chain_topk(const SampleParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_commit_kv(const CommitParams &p, int grid, cudaStream_t s);
 int commit_threads();
 size_t commit_smem_bytes(int B);

@@ -1,0 +1,750 @@
+// Device pieces shared by the sampled chain-verification kernels.
+//
+// verify_sample.cu runs one thread-block cluster per (position, request)
+// for full-vocabulary rows and for top-k rows whose threshold needs the
+// exact cluster-wide search; verify_topk.cu runs cluster-free blocks for
+// top-k rows.  Both end each position with masked_position() or
+// compact_position() below and finish() (record + request epilogue).
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "ddmath.cuh"
+#include "kernels.h"
+#include "select.cuh"
+#include "tma.cuh"
+
+namespace specv {
+
+namespace cg = cooperative_groups;
+
+constexpr int kNT = 256;
+constexpr int kNW = kNT / 32;
+constexpr int kMaxCluster = 8;
+constexpr int kSeg = 256;        // candidates one top-k slice may contribute per row
+constexpr int kScanE = 8;        // elements per thread per tile of the token-order scan
+constexpr int kKeptMax = 1024;   // kept (top-k) entries per row a position can sort
+constexpr int kPool = kTopKPool;  // top-k candidates per row a position can collect
+
+// Dynamic shared memory: full-vocab rows stream through a ring; top-k rows
+// stage the whole slice pair, later reused for the merge.
+constexpr int kRingCH = 8192, kRingNST = 4;
+constexpr int kFastStage = 32768;   // a top-k slice must fit in one stage per row
+using SampRing = Ring<kRingCH, kRingNST, 2>;
+using FastRing = Ring<kFastStage, 1, 2>;
+constexpr size_t kSampDyn = sizeof(SampRing) > sizeof(FastRing) ? sizeof(SampRing) : sizeof(FastRing);
+
+struct SampBase {
+    float2 red2[kNW];
+    float redf[kNW];
+    unsigned redu[kNW];
+    float4 redd[kNW];
+    float4 ms[kMaxCluster];       // pushed (m_p, s_p, m_q, s_q) per rank
+    float4 dsum[kMaxCluster];     // pushed dd pair of sums per rank
+    float zdiag[kMaxCluster];     // pushed fp32 residual mass per rank
+    unsigned cnt[2][2][kMaxCluster];
+    unsigned rej;                 // earliest-rejection word, pushed by rank 0
+    unsigned ovf;                 // candidate-list overflow, OR-ed by every rank
+    int found, lastpos, arrive_last;
+    unsigned hist[256];
+    unsigned bc[2];
+    unsigned tau[2];
+    float2 tab[65];
+    float2 ln2;
+};
+
+struct Outcome {
+    float a, z;
+    int token;
+    unsigned info;
+};
+
+template <typename T> __device__ __forceinline__ uint32_t kkey(float x) {
+    return fkey(x) >> (32 - Elem<T>::KEY_BITS);
+}
+template <typename T> __device__ __forceinline__ float key_value(uint32_t kk) {
+    const uint32_t f = kk << (32 - Elem<T>::KEY_BITS);
+    const uint32_t u = (f & 0x80000000u) ? (f & 0x7fffffffu) : ~f;
+    return __uint_as_float(Elem<T>::KEY_BITS == 16 ? (u & 0xffff0000u) : u);
+}
+
+// Two rows traversed together over one slice: f(xa[VEC], xb[VEC], base, cnt).
+template <typename T, int UNROLL, typename F>
+__device__ __forceinline__ void for_slice2(const T *ra, const T *rb, int lo, int hi, F &&f) {
+    constexpr int VEC = Elem<T>::VEC;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (hi <= lo) return;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ra + lo);
+    const bool same_phase = ((a ^ reinterpret_cast<uintptr_t>(rb + lo)) & 15u) == 0;
+    int head = (int)(((16u - (unsigned)(a & 15u)) & 15u) / sizeof(T));
+    if (head > hi - lo) head = hi - lo;
+    const int body0 = lo + head;
+    const int nvec = (hi - body0) / VEC;
+    const int tail0 = body0 + nvec * VEC;
+    if (tid < head) {
+        float xa[VEC], xb[VEC];
+        xa[0] = ld_elem(ra, lo + tid);
+        xb[0] = ld_elem(rb, lo + tid);
+        f(xa, xb, lo + tid, 1);
+    }
+    const uint4 *va = reinterpret_cast<const uint4 *>(ra + body0);
+    const uint4 *vb = reinterpret_cast<const uint4 *>(rb + body0);
+    int v = tid;
+    if (same_phase) {
+        for (; v + (UNROLL - 1) * nt < nvec; v += UNROLL * nt) {
+            uint4 qa[UNROLL], qb[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                qa[u] = ld_nc16(va + v + u * nt);
+                qb[u] = ld_nc16(vb + v + u * nt);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                float xa[VEC], xb[VEC];
+                unpack<T>(qa[u], xa);
+                unpack<T>(qb[u], xb);
+                f(xa, xb, body0 + (v + u * nt) * VEC, VEC);
+            }
+        }
+    }
+    for (; v < nvec; v += nt) {
+        float xa[VEC], xb[VEC];
+        unpack<T>(ld_nc16(va + v), xa);
+        const int base = body0 + v * VEC;
+        if (same_phase) {
+            unpack<T>(ld_nc16(vb + v), xb);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) xb[e] = ld_elem(rb, base + e);
+        }
+        f(xa, xb, base, VEC);
+    }
+    if (tid < hi - tail0) {
+        float xa[VEC], xb[VEC];
+        xa[0] = ld_elem(ra, tail0 + tid);
+        xb[0] = ld_elem(rb, tail0 + tid);
+        f(xa, xb, tail0 + tid, 1);
+    }
+}
+
+// Streams slice [lo, hi) of one row (drow == nullptr) or two rows: the scalar
+// head and tail from global memory, the 16-byte body through the bulk-copy
+// ring.  f(xa[VEC], xb[VEC], base, cnt) as in for_slice2.  Rows whose 16-byte
+// phases differ take the register path instead.  Returns false on a wait
+// timeout.
+template <typename T, typename F>
+__device__ bool stream_rows(SampRing &R, const T *trow, const T *drow, int lo, int hi, F &&f) {
+    constexpr int VEC = Elem<T>::VEC;
+    const int tid = threadIdx.x;
+    const SliceSplit sp = split_slice(trow, lo, hi);
+    const bool two = drow != nullptr;
+    const bool same = !two ||
+        ((reinterpret_cast<uintptr_t>(trow + lo) ^ reinterpret_cast<uintptr_t>(drow + lo)) & 15u) == 0;
+    if (!same) {
+        for_slice2<T, 2>(trow, drow, lo, hi, f);
+        return true;
+    }
+    const int nhead = sp.body0 - sp.head0, ntail = sp.hi - sp.tail0;
+    if (tid < nhead) {
+        float xa[VEC], xb[VEC];
+        xa[0] = ld_elem(trow, sp.head0 + tid);
+        xb[0] = two ? ld_elem(drow, sp.head0 + tid) : 0.0f;
+        f(xa, xb, sp.head0 + tid, 1);
+    }
+    bool ok = true;
+    const uint32_t nbytes = (uint32_t)((sp.tail0 - sp.body0) * (int)sizeof(T));
+    if (nbytes > 0) {
+        const unsigned char *src[2] = {reinterpret_cast<const unsigned char *>(trow + sp.body0),
+                                       two ? reinterpret_cast<const unsigned char *>(drow + sp.body0) : nullptr};
+        ok = ring_stream(R, src, two ? 2 : 1, nbytes,
+                         [&](const unsigned char *const *st, uint32_t off, uint32_t bytes) {
+            const uint4 *va = reinterpret_cast<const uint4 *>(st[0]);
+            const uint4 *vb = reinterpret_cast<const uint4 *>(st[1]);
+            const int nv = (int)(bytes / 16);
+            const int base0 = sp.body0 + (int)(off / sizeof(T));
+            for (int q = tid; q < nv; q += kNT) {
+                float xa[VEC], xb[VEC];
+                unpack<T>(va[q], xa);
+                if (two) unpack<T>(vb[q], xb);
+                f(xa, xb, base0 + q * VEC, VEC);
+            }
+        });
+    }
+    if (tid < ntail) {
+        float xa[VEC], xb[VEC];
+        xa[0] = ld_elem(trow, sp.tail0 + tid);
+        xb[0] = two ? ld_elem(drow, sp.tail0 + tid) : 0.0f;
+        f(xa, xb, sp.tail0 + tid, 1);
+    }
+    return ok;
+}
+
+// Online (max, sum) update of one row with one vector of values.
+template <int VEC, bool MASK>
+__device__ __forceinline__ void ms_update(MaxSum &ms, const float *x, int cnt, uint32_t th,
+                                          int ks, float c2) {
+    float vm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+        if (e < cnt && (!MASK || (fkey(x[e]) >> ks) >= th)) vm = fmaxf(vm, x[e]);
+    if (vm > ms.m) {
+        ms.s = ms.m == -INFINITY ? 0.0f : ms.s * exp2f((ms.m - vm) * c2);
+        ms.m = vm;
+    }
+    if (ms.m != -INFINITY) {
+        const float mc = ms.m * c2;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (e < cnt && (!MASK || (fkey(x[e]) >> ks) >= th)) ms.s += exp2f(fmaf(x[e], c2, -mc));
+    }
+}
+
+// block-wide dd sum of two accumulators (every thread gets both)
+template <int NT>
+__device__ __forceinline__ void block_dd_sum2(dd &a, dd &b, float4 *red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    a = warp_dd_sum(a);
+    b = warp_dd_sum(b);
+    __syncthreads();
+    if (lane == 0) red[w] = make_float4(a.hi, a.lo, b.hi, b.lo);
+    __syncthreads();
+    dd ta{0.0f, 0.0f}, tb{0.0f, 0.0f};
+    for (int i = 0; i < NT / 32; ++i) {
+        ta = dd_add(ta, dd{red[i].x, red[i].y});
+        tb = dd_add(tb, dd{red[i].z, red[i].w});
+    }
+    a = ta;
+    b = tb;
+}
+
+// ---------------------------------------------------------------------------
+// Token-order scan of one slice: the smallest i in [lo, hi) whose running sum
+// (starting at `carry`) exceeds t, among positive weights; if rounding leaves
+// none, the last positive-weight index.  weight(i) returns a dd.
+// ---------------------------------------------------------------------------
+template <int NT, typename W>
+__device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBase &sb) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) { sb.found = INT_MAX; sb.lastpos = -1; }
+    __syncthreads();
+    for (int base = lo; base < hi; base += NT * kScanE) {
+        const int i0 = base + tid * kScanE;
+        dd w[kScanE];
+        dd run{0.0f, 0.0f};
+        int lastp = -1;
+#pragma unroll
+        for (int e = 0; e < kScanE; ++e) {
+            const int i = i0 + e;
+            w[e] = i < hi ? weight(i) : dd{0.0f, 0.0f};
+            run = dd_add(run, w[e]);
+            if (dd_pos(w[e])) lastp = i;
+        }
+        // inclusive warp scan of the thread totals, then warp totals
+        dd incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const dd y{__shfl_up_sync(kFull, incl.hi, o), __shfl_up_sync(kFull, incl.lo, o)};
+            if (lane >= o) incl = dd_add(y, incl);
+        }
+        __syncthreads();
+        if (lane == 31) sb.redd[wid] = make_float4(incl.hi, incl.lo, 0.0f, 0.0f);
+        __syncthreads();
+        dd wpre{0.0f, 0.0f}, tile{0.0f, 0.0f};
+        for (int q = 0; q < NT / 32; ++q) {
+            const dd x{sb.redd[q].x, sb.redd[q].y};
+            if (q < wid) wpre = dd_add(wpre, x);
+            tile = dd_add(tile, x);
+        }
+        // exclusive prefix of this thread = carry + earlier warps + earlier lanes
+        const dd lane_excl{__shfl_up_sync(kFull, incl.hi, 1), __shfl_up_sync(kFull, incl.lo, 1)};
+        dd cum = dd_add(carry, wpre);
+        if (lane > 0) cum = dd_add(cum, lane_excl);
+        int hit = INT_MAX;
+#pragma unroll
+        for (int e = 0; e < kScanE; ++e) {
+            cum = dd_add(cum, w[e]);
+            if (hit == INT_MAX && dd_pos(w[e]) && dd_gt(cum, t)) hit = i0 + e;
+        }
+        if (hit != INT_MAX) atomicMin(&sb.found, hit);
+        if (lastp >= 0) atomicMax(&sb.lastpos, lastp);
+        __syncthreads();
+        if (sb.found != INT_MAX) break;
+        carry = dd_add(carry, tile);
+    }
+    return sb.found != INT_MAX ? sb.found : sb.lastpos;
+}
+
+// ---------------------------------------------------------------------------
+// The request epilogue: the last position to arrive writes the outputs.
+// ---------------------------------------------------------------------------
+static __device__ void write_request(const SampleParams &p, int b) {
+    const int g = p.gamma;
+    __threadfence();
+    const volatile PosRec *R = p.recs + (int64_t)b * (g + 1);
+    unsigned badbits = 0;
+    for (int q = 0; q <= g; ++q) {
+        const unsigned info = R[q].info;
+        badbits |= (info & REC_BAD_INPUT) ? SPEC_FLAG_BAD_INPUT : 0u;
+        badbits |= (info & REC_BAD_ROW) ? SPEC_FLAG_BAD_ROW : 0u;
+    }
+    if (badbits) {
+        p.n_acc[b] = 0;
+        p.n_out[b] = 0;
+        if (p.flags) p.flags[b] = badbits;
+        atomicOr(p.status, badbits);
+    } else {
+        int n = g;
+        for (int q = 0; q < g; ++q)
+            if (!(R[q].info & REC_ACCEPT)) { n = q; break; }
+        int *out = p.out_tokens + (int64_t)b * (g + 1);
+        const int *dt = p.tokens + (int64_t)b * g;
+        for (int q = 0; q < n; ++q) out[q] = dt[q];
+        out[n] = R[n].token;
+        p.n_acc[b] = n;
+        p.n_out[b] = n + 1;
+        if (p.accept_prob)
+            for (int q = 0; q < g; ++q) p.accept_prob[(int64_t)b * g + q] = R[q].a;
+        if (p.resid)
+            for (int q = 0; q < g; ++q) p.resid[(int64_t)b * g + q] = R[q].z;
+        if (p.flags) p.flags[b] = (R[n].info & REC_FALLBACK) ? SPEC_FLAG_FALLBACK : 0u;
+    }
+    p.rejword[b] = 0u;
+    p.counters[b] = 0u;
+}
+
+static __device__ void finish(const SampleParams &p, int b, int k, const Outcome &o, SampBase &sb) {
+    if (threadIdx.x == 0) {
+        PosRec rec;
+        rec.a = o.a;
+        rec.z = o.z;
+        rec.token = o.token;
+        rec.info = o.info;
+        p.recs[(int64_t)b * (p.gamma + 1) + k] = rec;
+        __threadfence();
+        sb.arrive_last = atomicAdd(p.counters + b, 1u) == (unsigned)p.gamma;
+        if (sb.arrive_last) write_request(p, b);
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Exchange between the CTAs that share one position: a real thread-block
+// cluster (DSMEM pushes, cluster barriers) or a single CTA doing the whole row.
+// ---------------------------------------------------------------------------
+struct ClusterEx {
+    cg::cluster_group cl;
+    int c, j;
+    bool waited;
+    __device__ ClusterEx(int c_, int j_) : cl(cg::this_cluster()), c(c_), j(j_), waited(false) {}
+    // the kernel arrived on the cluster barrier at its start; wait once
+    // before the first remote write so every CTA of the cluster is running
+    __device__ void ready() {
+        if (!waited) {
+            asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+            waited = true;
+        }
+    }
+    template <class P> __device__ P *at(P *local, int r) { return cl.map_shared_rank(local, r); }
+    __device__ void sync() { cl.sync(); }
+};
+
+struct SoloEx {
+    int c = 1, j = 0;
+    __device__ void ready() {}
+    template <class P> __device__ P *at(P *local, int) { return local; }
+    __device__ void sync() { __syncthreads(); }
+};
+
+// ---------------------------------------------------------------------------
+// One position over the exchange `ex`: optional exact top-k threshold by a
+// binary search on order keys (MASK), pass 1 (online max/sum, bulk-copy
+// ring), acceptance, optional fp32 residual mass, and the double-float draw
+// where this position decides the emitted token.  Every CTA of the exchange
+// runs it on its slice [lo, hi); the CTA that ends up holding the whole
+// outcome calls finish().
+// ---------------------------------------------------------------------------
+template <typename T, bool MASK, typename Ex>
+__device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned char *dsm, Ex &ex,
+                                int k, int b, int lo, int hi) {
+    constexpr int VEC = Elem<T>::VEC;
+    constexpr int KB = Elem<T>::KEY_BITS;
+    constexpr int KS = 32 - KB;
+    const int tid = threadIdx.x, c = ex.c, j = ex.j, g = p.gamma;
+    const bool has_draft = k < g;
+    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
+    const T *drow = has_draft
+        ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
+    const float c2 = p.c2;
+    const dd c2d{p.c2_hi, p.c2_lo};
+    const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
+    const bool bad_tok = has_draft && (d < 0 || d >= p.V);
+    const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
+    const float g_d = (has_draft && !bad_tok) ? ld_elem(drow, d) : 0.0f;
+    const float u_k = has_draft ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
+    const float u_f = p.unif[(int64_t)b * (g + 1) + g];
+    Outcome o{1.0f, 0.0f, -1, 0u};
+
+    uint32_t th_p = 0u, th_q = 0u;
+    if (MASK) {
+        uint32_t lo_p = 0u, hi_p = KB == 32 ? 0xffffffffu : ((1u << KB) - 1u);
+        uint32_t lo_q = 0u, hi_q = has_draft ? hi_p : 0u;
+        const unsigned K = (unsigned)p.top_k;
+        for (int it = 0; it < KB; ++it) {
+            const bool act_p = lo_p < hi_p, act_q = lo_q < hi_q;
+            if (!act_p && !act_q) break;  // identical in every CTA of the exchange
+            const uint32_t mid_p = lo_p + (uint32_t)(((uint64_t)hi_p - lo_p + 1) >> 1);
+            const uint32_t mid_q = lo_q + (uint32_t)(((uint64_t)hi_q - lo_q + 1) >> 1);
+            unsigned cp = 0, cq = 0;
+            if (act_p)
+                for_slice<T, 4>(trow, lo, hi, tid, kNT, [&](float x, int) { cp += (fkey(x) >> KS) >= mid_p; });
+            if (act_q)
+                for_slice<T, 4>(drow, lo, hi, tid, kNT, [&](float x, int) { cq += (fkey(x) >> KS) >= mid_q; });
+            cp = block_sum_u<kNT>(cp, sb.redu);
+            cq = block_sum_u<kNT>(cq, sb.redu);
+            const int par = it & 1;
+            ex.ready();
+            if (tid < c) {
+                unsigned *dst = ex.at(&sb.cnt[par][0][0], tid);
+                dst[j] = cp;
+                dst[kMaxCluster + j] = cq;
+            }
+            ex.sync();
+            unsigned tp = 0, tq = 0;
+            for (int r = 0; r < c; ++r) {
+                tp += sb.cnt[par][0][r];
+                tq += sb.cnt[par][1][r];
+            }
+            if (act_p) { if (tp >= K) lo_p = mid_p; else hi_p = mid_p - 1; }
+            if (act_q) { if (tq >= K) lo_q = mid_q; else hi_q = mid_q - 1; }
+        }
+        th_p = lo_p;
+        th_q = lo_q;
+    }
+
+    // ---- pass 1 (HBM): online max / sum of the kept logits -------------------
+    MaxSum msp{-INFINITY, 0.0f}, msq{-INFINITY, 0.0f};
+    {
+        SampRing &R = *reinterpret_cast<SampRing *>(dsm);
+        const bool okc = stream_rows<T>(R, trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+            ms_update<VEC, MASK>(msp, xa, cnt, th_p, KS, c2);
+            if (has_draft) ms_update<VEC, MASK>(msq, xb, cnt, th_q, KS, c2);
+        });
+        if (!okc && tid == 0) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+    }
+    msp = block_ms<kNT>(msp, c2, sb.red2);
+    msq = block_ms<kNT>(msq, c2, sb.red2);
+    unsigned prior = 0u;
+    if (j == 0 && tid == 0) prior = *((volatile unsigned *)&p.rejword[b]);
+    ex.ready();
+    if (tid < c) {
+        float4 *dst = ex.at(&sb.ms[0], tid);
+        dst[j] = make_float4(msp.m, msp.s, msq.m, msq.s);
+    }
+    if (j == 0 && tid == 0)
+        for (int r = 0; r < c; ++r) *ex.at(&sb.rej, r) = prior;
+    ex.sync();
+    MaxSum Mp{-INFINITY, 0.0f}, Mq{-INFINITY, 0.0f};
+    for (int r = 0; r < c; ++r) {
+        Mp = ms_combine(Mp, MaxSum{sb.ms[r].x, sb.ms[r].y}, c2);
+        Mq = ms_combine(Mq, MaxSum{sb.ms[r].z, sb.ms[r].w}, c2);
+    }
+    const bool bad_row = Mp.m == -INFINITY || (has_draft && Mq.m == -INFINITY);
+    const bool bad = bad_tok || bad_row;
+    o.info = (bad_tok ? REC_BAD_INPUT : 0u) | (bad_row ? REC_BAD_ROW : 0u);
+    bool accept = false;
+    if (has_draft && !bad) {
+        const float mcp = Mp.m * c2, mcq = Mq.m * c2;
+        const float pd = (!MASK || (fkey(l_d) >> KS) >= th_p) ? exp2f(fmaf(l_d, c2, -mcp)) / Mp.s : 0.0f;
+        const float qd = (!MASK || (fkey(g_d) >> KS) >= th_q) ? exp2f(fmaf(g_d, c2, -mcq)) / Mq.s : 0.0f;
+        o.a = qd > 0.0f ? fminf(1.0f, pd / qd) : (pd > 0.0f ? 1.0f : 0.0f);
+        accept = u_k < o.a;
+        o.info |= accept ? REC_ACCEPT : 0u;
+    }
+    const bool earlier = sb.rej > (unsigned)(g - k + 1);
+    if (has_draft && !bad && !accept && j == 0 && tid == 0) atomicMax(p.rejword + b, (unsigned)(g - k + 1));
+    const bool draw = !bad && (!has_draft || !accept) && !earlier;
+    int writer = 0;
+
+    if (!draw && has_draft && !bad && p.resid) {
+        // ---- diagnostic residual mass in fp32 (pass 2, L2) ----
+        const float mcp = Mp.m * c2, mcq = Mq.m * c2, isp = 1.0f / Mp.s, isq = 1.0f / Mq.s;
+        float zw = 0.0f;
+        for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                if (e < cnt) {
+                    // explicit roundings: no fused multiply-add may turn p_i - q_i for
+                    // identical rows into a rounding residue
+                    const float pi = (!MASK || (fkey(xa[e]) >> KS) >= th_p) ? __fmul_rn(exp2f(fmaf(xa[e], c2, -mcp)), isp) : 0.0f;
+                    const float qi = (!MASK || (fkey(xb[e]) >> KS) >= th_q) ? __fmul_rn(exp2f(fmaf(xb[e], c2, -mcq)), isq) : 0.0f;
+                    zw += fmaxf(pi - qi, 0.0f);
+                }
+            }
+        });
+        zw = block_sum<kNT>(zw, sb.redf);
+        if (tid < c) *ex.at(&sb.zdiag[j], tid) = zw;
+        ex.sync();
+        float z = 0.0f;
+        for (int r = 0; r < c; ++r) z += sb.zdiag[r];
+        o.z = z;
+    }
+
+    if (draw) {
+        // ---- the draw in dd: slice sums (pass A), residual (pass B), scan ----
+        const float2 *tab = sb.tab;
+        const float2 ln2 = sb.ln2;
+        const float mp = Mp.m, mq = Mq.m;
+        auto ep = [&](float x) -> dd {
+            return (!MASK || (fkey(x) >> KS) >= th_p) ? dd_expw(x, mp, c2d, tab, ln2) : dd{0.0f, 0.0f};
+        };
+        auto eq = [&](float y) -> dd {
+            return (!MASK || (fkey(y) >> KS) >= th_q) ? dd_expw(y, mq, c2d, tab, ln2) : dd{0.0f, 0.0f};
+        };
+        dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f};
+        if (has_draft) {
+            for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    if (e < cnt) {
+                        sp = dd_add(sp, ep(xa[e]));
+                        sq = dd_add(sq, eq(xb[e]));
+                    }
+                }
+            });
+        } else {
+            for_slice_vec<T, 4>(trow, lo, hi, tid, kNT, [&](const float *x, int, int cnt) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (e < cnt) sp = dd_add(sp, ep(x[e]));
+            });
+        }
+        block_dd_sum2<kNT>(sp, sq, sb.redd);
+        if (tid < c) *ex.at(&sb.dsum[j], tid) = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
+        ex.sync();
+        dd Sp{0.0f, 0.0f}, Sq{0.0f, 0.0f};
+        float4 part[kMaxCluster];
+        for (int r = 0; r < c; ++r) {
+            Sp = dd_add(Sp, dd{sb.dsum[r].x, sb.dsum[r].y});
+            Sq = dd_add(Sq, dd{sb.dsum[r].z, sb.dsum[r].w});
+            part[r] = sb.dsum[r];
+        }
+        const dd isp = dd_recip(Sp);
+        const dd isq = has_draft ? dd_recip(Sq) : dd{0.0f, 0.0f};
+        bool use_p = true, fb = false;
+        dd total = Sp;  // bonus: weights are the unnormalised target terms
+        if (has_draft) {
+            dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
+            for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    if (e < cnt) {
+                        const dd pi = dd_mul(ep(xa[e]), isp);
+                        const dd qi = dd_mul(eq(xb[e]), isq);
+                        zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qi))));
+                        zp = dd_add(zp, pi);
+                    }
+                }
+            });
+            block_dd_sum2<kNT>(zw, zp, sb.redd);
+            __syncthreads();
+            if (tid < c) *ex.at(&sb.dsum[j], tid) = make_float4(zw.hi, zw.lo, zp.hi, zp.lo);
+            ex.sync();
+            dd Zw{0.0f, 0.0f}, Zp{0.0f, 0.0f};
+            for (int r = 0; r < c; ++r) {
+                Zw = dd_add(Zw, dd{sb.dsum[r].x, sb.dsum[r].y});
+                Zp = dd_add(Zp, dd{sb.dsum[r].z, sb.dsum[r].w});
+                part[r] = sb.dsum[r];
+            }
+            o.z = dd_to_f(Zw);
+            fb = dd_le(Zw, dd{p.eps, 0.0f});
+            use_p = fb;
+            total = fb ? Zp : Zw;
+            if (fb) o.info |= REC_FALLBACK;
+        }
+        const dd t = dd_mul_f(total, u_f);
+        // the slice that holds the crossing (identical choice in every CTA)
+        int owner = -1, lastpos = -1;
+        dd acc{0.0f, 0.0f}, own_prefix{0.0f, 0.0f}, last_prefix{0.0f, 0.0f};
+        for (int r = 0; r < c; ++r) {
+            const dd prt = !has_draft ? dd{part[r].x, part[r].y}
+                                      : (use_p ? dd{part[r].z, part[r].w} : dd{part[r].x, part[r].y});
+            if (dd_pos(prt)) {
+                if (owner < 0 && dd_gt(dd_add(acc, prt), t)) { owner = r; own_prefix = acc; }
+                lastpos = r;
+                last_prefix = acc;
+            }
+            acc = dd_add(acc, prt);
+        }
+        if (owner < 0) { owner = lastpos; own_prefix = last_prefix; }
+        writer = owner < 0 ? 0 : owner;
+        if (j == owner) {
+            o.token = dd_scan_slice<kNT>(lo, hi, own_prefix, t, [&](int i) -> dd {
+                const dd e = ep(ld_elem(trow, i));
+                if (!has_draft) return e;
+                const dd pi = dd_mul(e, isp);
+                if (use_p) return pi;
+                return dd_max0(dd_add(pi, dd_neg(dd_mul(eq(ld_elem(drow, i)), isq))));
+            }, sb);
+        }
+    }
+    if (j == writer) finish(p, b, k, o, sb);
+}
+
+// ---------------------------------------------------------------------------
+// One top-k position from candidate lists already in shared memory: list r
+// (row 0 = target, 1 = draft) holds n[r] entries (order key, token id) that
+// include every logit >= the row's k-th largest.  The exact threshold comes
+// from a block select, the kept set is sorted by token id (so every later
+// sum runs in a fixed order), and acceptance, residual mass and the draw are
+// computed in double-float over the kept sets.  `work` is shared memory for
+// 3 * kKeptMax entries.  One CTA; it calls finish().  A kept set larger than
+// kKeptMax (massive ties) falls back to masked_position over the whole row
+// in this block (`solo` exchange; `dsm` is then its streaming ring).
+// ---------------------------------------------------------------------------
+template <typename T, typename Solo>
+__device__ void compact_position(const SampleParams &p, SampBase &sb, const uint2 *const *lists,
+                                 const int *n, uint2 *work, unsigned char *dsm, Solo &solo, int k,
+                                 int b) {
+    constexpr int KB = Elem<T>::KEY_BITS;
+    const int tid = threadIdx.x, g = p.gamma;
+    const bool has_draft = k < g;
+    const T *drow = has_draft
+        ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
+    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
+    const dd c2d{p.c2_hi, p.c2_lo};
+    const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
+    const bool bad_tok = has_draft && (d < 0 || d >= p.V);
+    const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
+    const float g_d = (has_draft && !bad_tok) ? ld_elem(drow, d) : 0.0f;
+    const float u_k = has_draft ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
+    const float u_f = p.unif[(int64_t)b * (g + 1) + g];
+    Outcome o{1.0f, 0.0f, -1, 0u};
+    const int rows = has_draft ? 2 : 1;
+    __shared__ int s_kn[2];
+    uint32_t th[2] = {0u, 0u};
+    unsigned kn[2] = {0u, 0u};
+    for (int r = 0; r < rows; ++r) {
+        const uint2 *L = lists[r];
+        const int nr = n[r];
+        th[r] = block_kth_largest<KB, kNT>(
+            [&](auto &&f) { for (int x = tid; x < nr; x += kNT) f(L[x].x); },
+            (unsigned)min(p.top_k, nr), sb.hist, sb.bc);
+        unsigned cnt = 0;
+        for (int x = tid; x < nr; x += kNT) cnt += L[x].x >= th[r];
+        kn[r] = block_sum_u<kNT>(cnt, sb.redu);
+    }
+    if (kn[0] > (unsigned)kKeptMax || kn[1] > (unsigned)kKeptMax) {
+        // hundreds of logits tied at the threshold: the exact masked path over
+        // the whole row in this one block
+        masked_position<T, true>(p, sb, dsm, solo, k, b, 0, p.V);
+        return;
+    }
+    uint2 *sorted[2] = {work, work + kKeptMax};
+    uint2 *tmp = work + 2 * kKeptMax;  // free until the draw
+    for (int r = 0; r < rows; ++r) {
+        // compact the kept entries, then place each at its rank in token order
+        // (rank = number of kept entries with a smaller id; ids are distinct)
+        const uint2 *L = lists[r];
+        const int nr = n[r];
+        if (tid == 0) s_kn[r] = 0;
+        __syncthreads();
+        for (int x = tid; x < nr; x += kNT) {
+            const uint2 e = L[x];
+            if (e.x >= th[r]) tmp[atomicAdd(&s_kn[r], 1)] = e;
+        }
+        __syncthreads();
+        const int m = (int)kn[r];
+        for (int x = tid; x < m; x += kNT) {
+            const uint2 e = tmp[x];
+            int rank = 0;
+            for (int y = 0; y < m; ++y) rank += tmp[y].y < e.y;
+            sorted[r][rank] = e;
+        }
+        __syncthreads();
+    }
+    // row statistics in dd over the kept sets (fixed order per thread)
+    const float2 *tab = sb.tab;
+    const float2 ln2 = sb.ln2;
+    const uint2 *Kp = sorted[0];
+    const uint2 *Kq = sorted[1];
+    const int np = s_kn[0], nq = rows == 2 ? s_kn[1] : 0;
+    float mp = -INFINITY, mq = -INFINITY;
+    for (int i = tid; i < np; i += kNT) mp = fmaxf(mp, key_value<T>(Kp[i].x));
+    for (int i = tid; i < nq; i += kNT) mq = fmaxf(mq, key_value<T>(Kq[i].x));
+    mp = block_ms<kNT>(MaxSum{mp, 0.0f}, 1.0f, sb.red2).m;
+    mq = block_ms<kNT>(MaxSum{mq, 0.0f}, 1.0f, sb.red2).m;
+    const bool bad_row = mp == -INFINITY || (has_draft && mq == -INFINITY);
+    dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f};
+    if (!bad_row) {
+        for (int i = tid; i < np; i += kNT) sp = dd_add(sp, dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2));
+        for (int i = tid; i < nq; i += kNT) sq = dd_add(sq, dd_expw(key_value<T>(Kq[i].x), mq, c2d, tab, ln2));
+    }
+    block_dd_sum2<kNT>(sp, sq, sb.redd);
+    const bool bad = bad_tok || bad_row;
+    o.info = (bad_tok ? REC_BAD_INPUT : 0u) | (bad_row ? REC_BAD_ROW : 0u);
+    if (!bad) {
+        const dd isp = dd_recip(sp);
+        const dd isq = has_draft ? dd_recip(sq) : dd{0.0f, 0.0f};
+        bool accept = false;
+        if (has_draft) {
+            const dd pd = kkey<T>(l_d) >= th[0] ? dd_mul(dd_expw(l_d, mp, c2d, tab, ln2), isp) : dd{0.0f, 0.0f};
+            const dd qd = kkey<T>(g_d) >= th[1] ? dd_mul(dd_expw(g_d, mq, c2d, tab, ln2), isq) : dd{0.0f, 0.0f};
+            float a;
+            if (dd_pos(qd)) {
+                const dd ratio = dd_mul(pd, dd_recip(qd));
+                a = dd_gt(ratio, dd{1.0f, 0.0f}) ? 1.0f : dd_to_f(ratio);
+            } else {
+                a = dd_pos(pd) ? 1.0f : 0.0f;
+            }
+            o.a = a;
+            accept = u_k < a;
+            o.info |= accept ? REC_ACCEPT : 0u;
+        }
+        // residual weights over the target's kept set (q gathered from the draft row)
+        auto qprob = [&](int idx) -> dd {
+            const float y = ld_elem(drow, idx);
+            return kkey<T>(y) >= th[1] ? dd_mul(dd_expw(y, mq, c2d, tab, ln2), isq) : dd{0.0f, 0.0f};
+        };
+        dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
+        if (has_draft) {
+            for (int i = tid; i < np; i += kNT) {
+                const dd pi = dd_mul(dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2), isp);
+                zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qprob((int)Kp[i].y)))));
+                zp = dd_add(zp, pi);
+            }
+            block_dd_sum2<kNT>(zw, zp, sb.redd);
+            o.z = dd_to_f(zw);
+        }
+        if (tid == 0) sb.rej = *((volatile unsigned *)&p.rejword[b]);
+        __syncthreads();
+        const bool earlier = sb.rej > (unsigned)(g - k + 1);
+        if (has_draft && !accept && tid == 0) atomicMax(p.rejword + b, (unsigned)(g - k + 1));
+        if ((!has_draft || !accept) && !earlier) {
+            // ---- the draw, in token order over the kept set ----
+            const bool fb = has_draft && dd_le(zw, dd{p.eps, 0.0f});
+            if (fb) o.info |= REC_FALLBACK;
+            const bool use_p = !has_draft || fb;
+            const dd total = !has_draft ? sp : (fb ? zp : zw);
+            const dd t = dd_mul_f(total, u_f);
+            // the kept set is already in token order
+            float2 *ws = reinterpret_cast<float2 *>(work + 2 * kKeptMax);
+            __syncthreads();
+            for (int i = tid; i < np; i += kNT) {
+                dd wgt = dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2);
+                if (has_draft) {
+                    wgt = dd_mul(wgt, isp);
+                    if (!use_p) wgt = dd_max0(dd_add(wgt, dd_neg(qprob((int)Kp[i].y))));
+                }
+                ws[i] = make_float2(wgt.hi, wgt.lo);
+            }
+            __syncthreads();
+            o.token = dd_scan_slice<kNT>(0, np, dd{0.0f, 0.0f}, t,
+                                         [&](int i) { return dd{ws[i].x, ws[i].y}; }, sb);
+            if (o.token >= 0) o.token = (int)Kp[o.token].y;
+        }
+    }
+    finish(p, b, k, o, sb);
+}
+
+}  // namespace specv

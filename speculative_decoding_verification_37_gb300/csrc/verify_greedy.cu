@@ -14,6 +14,7 @@
 // ever waits on another.
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace specv {
 
@@ -147,60 +148,118 @@ __device__ void tree_epilogue(const ArgmaxParams &p, int b) {
 }
 
 // -- the pass ---------------------------------------------------------------------
+// The block's slice (<= 64 KiB) is staged in shared memory by bulk copies;
+// two shared-memory passes then find the largest value and the lowest index
+// holding it.
+constexpr int kArgStage = 65536;
+using ArgRing = Ring<kArgStage, 1, 1>;
+
 template <typename T>
 __global__ void __launch_bounds__(kArgNT) argmax_verify_kernel(ArgmaxParams p) {
+    constexpr int VEC = Elem<T>::VEC;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    ArgRing &R = *reinterpret_cast<ArgRing *>(dsm);
+    const int tid = threadIdx.x;
     const int slice = blockIdx.x % p.slices;
     const int row = blockIdx.x / p.slices;
     const int req = row / p.rows_per_req;
     const T *r = reinterpret_cast<const T *>(p.rows) + (int64_t)row * p.stride;
     const int lo = min(p.V, slice * p.slice_len);
     const int hi = min(p.V, lo + p.slice_len);
+    const SliceSplit sp = split_slice(r, lo, hi);
+    // scalar head and tail elements, one per thread at most
+    const int nhead = sp.body0 - sp.head0, ntail = sp.hi - sp.tail0;
+    const float xh = tid < nhead ? ld_elem(r, sp.head0 + tid) : -INFINITY;
+    const float xt = tid < ntail ? ld_elem(r, sp.tail0 + tid) : -INFINITY;
 
-    // each thread visits its elements in increasing index order, so a strict
-    // ">" keeps the lowest index among equal values
-    ArgMax best{-INFINITY, -1};
-    for_slice_vec<T, 4>(r, lo, hi, threadIdx.x, kArgNT, [&](const float *x, int base, int cnt) {
-#pragma unroll
-        for (int e = 0; e < Elem<T>::VEC; ++e)
-            if (e < cnt && (best.idx < 0 || x[e] > best.v)) best = ArgMax{x[e], base + e};
-    });
     __shared__ float s_v[kArgNT / 32];
-    __shared__ int s_i[kArgNT / 32];
     __shared__ int s_last;
-    best = warp_argmax(best);
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    if (lane == 0) {
-        s_v[w] = best.v;
-        s_i[w] = best.idx;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        ArgMax t = lane < kArgNT / 32 ? ArgMax{s_v[lane], s_i[lane]} : ArgMax{-INFINITY, -1};
-        t = warp_argmax(t);
-        if (lane == 0) {
-            if (t.idx >= 0) atomicMax(p.keys + row, argmax_key(t.v, t.idx));
-            __threadfence();
-            const unsigned prev = atomicAdd(p.counters + req, 1u);
-            s_last = prev == (unsigned)(p.slices * p.rows_per_req - 1);
+    __shared__ float s_max;
+    __shared__ int s_min;
+    const int lane = tid & 31, w = tid >> 5;
+    int bestidx = INT_MAX;
+    bool has = hi > lo;
+    auto passes = [&](const uint4 *v, int nv) {
+        // pass 1: the largest value of the slice
+        float m = fmaxf(xh, xt);
+        for (int q = tid; q < nv; q += kArgNT) {
+            float x[VEC];
+            unpack<T>(v[q], x);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[e]);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        if (lane == 0) s_v[w] = m;
+        __syncthreads();
+        if (tid == 0) {
+            float t = s_v[0];
+            for (int q = 1; q < kArgNT / 32; ++q) t = fmaxf(t, s_v[q]);
+            s_max = t;
+            s_min = INT_MAX;
+        }
+        __syncthreads();
+        const float M = s_max;
+        // pass 2: the lowest index holding it (-0 and +0 compare equal)
+        int mine = INT_MAX;
+        if (tid < nhead && xh == M) mine = sp.head0 + tid;
+        for (int q = tid; q < nv && mine == INT_MAX; q += kArgNT) {
+            float x[VEC];
+            unpack<T>(v[q], x);
+#pragma unroll
+            for (int e = VEC - 1; e >= 0; --e)
+                if (x[e] == M) mine = sp.body0 + q * VEC + e;
+        }
+        if (mine == INT_MAX && tid < ntail && xt == M) mine = sp.tail0 + tid;
+        if (mine != INT_MAX) atomicMin(&s_min, mine);
+        __syncthreads();
+        bestidx = s_min;
+    };
+    const uint32_t nbytes = (uint32_t)((sp.tail0 - sp.body0) * sizeof(T));
+    bool ok = true;
+    if (nbytes > 0) {
+        // the host keeps every slice within one stage, so this is one chunk
+        const unsigned char *src[1] = {reinterpret_cast<const unsigned char *>(r + sp.body0)};
+        ok = ring_stream(R, src, 1, nbytes, [&](const unsigned char *const *st, uint32_t, uint32_t bytes) {
+            passes(reinterpret_cast<const uint4 *>(st[0]), (int)(bytes / 16));
+        });
+    } else {
+        passes(nullptr, 0);
+    }
+    if (!ok && tid == 0) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+    if (tid == 0) {
+        if (has && bestidx != INT_MAX) atomicMax(p.keys + row, argmax_key(s_max, bestidx));
+        __threadfence();
+        const unsigned prev = atomicAdd(p.counters + req, 1u);
+        s_last = prev == (unsigned)(p.slices * p.rows_per_req - 1);
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     if (p.mode == 0) {
-        if (threadIdx.x == 0) greedy_chain_epilogue(p, req);
+        if (tid == 0) greedy_chain_epilogue(p, req);
     } else {
         tree_epilogue(p, req);
     }
-    if (threadIdx.x == 0) p.counters[req] = 0u;
+    if (tid == 0) p.counters[req] = 0u;
 }
+
+size_t argmax_smem_bytes() { return sizeof(ArgRing); }
 
 cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, cudaStream_t s) {
     const dim3 grid((unsigned)((int64_t)n_rows * p.slices));
-    if (dtype == SPEC_DTYPE_BF16)
-        argmax_verify_kernel<__nv_bfloat16><<<grid, kArgNT, 0, s>>>(p);
-    else
-        argmax_verify_kernel<float><<<grid, kArgNT, 0, s>>>(p);
+    const int smem = (int)sizeof(ArgRing);
+    static std::atomic<unsigned long long> done_bf16{0}, done_f32{0};
+    cudaError_t e;
+    if (dtype == SPEC_DTYPE_BF16) {
+        e = ensure_smem_attr(argmax_verify_kernel<__nv_bfloat16>, smem, done_bf16);
+        if (e != cudaSuccess) return e;
+        argmax_verify_kernel<__nv_bfloat16><<<grid, kArgNT, smem, s>>>(p);
+    } else {
+        e = ensure_smem_attr(argmax_verify_kernel<float>, smem, done_f32);
+        if (e != cudaSuccess) return e;
+        argmax_verify_kernel<float><<<grid, kArgNT, smem, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -138,7 +138,7 @@ def test_repeat_calls_are_deterministic_and_leave_workspace_zeroed():
     for key in ("n_acc", "out_tokens", "n_out", "accept_prob", "residual_mass", "flags"):
         np.testing.assert_array_equal(a[key], b[key])
     from speculative_decoding_verification_37_gb300 import api, _lib as L
-    ws = api.workspace(L.SPEC_WS_CHAIN, 8, 4, 20000, "cuda")
+    ws = api.workspace(L.SPEC_WS_CHAIN_TOPK, 8, 4, 20000, "cuda")
     torch.cuda.synchronize()
     counters = ws[256:256 + 8 * 4].view(torch.int32)
     assert int(counters.abs().sum()) == 0
