@@ -439,6 +439,7 @@ def main():
         args.warmup = 3
 
     from speculative_decoding_verification_37_gb300 import build as _b
+    from speculative_decoding_verification_37_gb300 import _lib as L
     _b.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -480,7 +481,12 @@ def main():
     peak, peak_kind = measured_peaks()
     t_verify = statistics.mean(verify_ms)
     achieved = wl.logit_bytes / (t_verify * 1e-3) / 1e9
-    kname = "argmax_verify_kernel" if (wl.kind == "tree" or wl.spec.greedy) else "chain_sample_kernel"
+    if wl.kind == "tree" or wl.spec.greedy:
+        kname = "argmax_verify_kernel"
+    elif 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
+        kname = "chain_topk_kernel"
+    else:
+        kname = "chain_sample_kernel"
     tr = traffic_record(kname)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -202,6 +202,9 @@ int spec_verify_tree(const SpecTreeArgs *args, void *workspace, size_t workspace
  *   (SPEC_FLAG_BAD_INPUT) if any slot id is outside [0,S), n_slots outside
  *   [0,S], the new length exceeds max_blocks*block_size or a block id it
  *   needs is outside [0,num_blocks).
+ * Workspace: spec_workspace_bytes(SPEC_WS_COMMIT, B, 0, 0) bytes (one
+ *   arrival counter per request), zero before the first call; every call
+ *   leaves it zero.
  */
 typedef struct SpecCommitArgs {
     int32_t B, L, H, D, S, block_size, elem_bytes;

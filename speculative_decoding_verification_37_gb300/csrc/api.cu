@@ -55,14 +55,21 @@ struct Ws {
     unsigned *counters;  // [B] arrival counters
     unsigned *rejword;   // [B] earliest rejection per request (chain, sampled)
     void *data;          // chain: records or argmax keys; tree: argmax keys
-    unsigned *poscnt;    // chain: [B*(gamma+1)] top-k arrivals per position
-    unsigned *poolcnt;   // chain: [B*(gamma+1)][2]
-    uint2 *pool;         // chain: [B*(gamma+1)][2][kTopKPool]
+    uint2 *slicecb;      // chain, top-k: [B*(gamma+1)][2][cmax] (count, bound key)
+    uint2 *pool;         // chain, top-k: [B*(gamma+1)][2][cmax][kTopKSlicePool]
 };
 
 // One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
 // (0 for other kinds), `data_bytes` the per-row keys or records.
-size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_ptr, bool with_pool) {
+// Slices per row of the top-k path; the workspace is sized for the larger
+// count (fp32 rows), so one size serves both element types.
+int topk_slices(int V, int dtype) { return slices_for(V, dtype, 1 << 20, topk_row_bytes()); }
+
+// One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
+// (0 for other kinds), `data_bytes` the per-row keys or records; with_pool
+// adds the top-k candidate regions for rows of V logits.
+size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_ptr, bool with_pool,
+                       int V = 0) {
     char *base = static_cast<char *>(base_ptr);
     size_t off = kWsHeader;
     const size_t per_req = ws_align((size_t)B * sizeof(unsigned));
@@ -75,15 +82,14 @@ size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_
     if (w) w->data = base + off;
     off += ws_align(data_bytes);
     if (!with_pool) {
-        if (w) w->poscnt = w->poolcnt = nullptr, w->pool = nullptr;
+        if (w) w->slicecb = nullptr, w->pool = nullptr;
         return off;
     }
-    if (w) w->poscnt = reinterpret_cast<unsigned *>(base + off);
-    off += ws_align(rows * sizeof(unsigned));
-    if (w) w->poolcnt = reinterpret_cast<unsigned *>(base + off);
-    off += ws_align(rows * 2 * sizeof(unsigned));
+    const size_t cmax = (size_t)topk_slices(V, SPEC_DTYPE_F32);
+    if (w) w->slicecb = reinterpret_cast<uint2 *>(base + off);
+    off += ws_align(rows * 2 * cmax * sizeof(uint2));
     if (w) w->pool = reinterpret_cast<uint2 *>(base + off);
-    off += ws_align(rows * 2 * (size_t)kTopKPool * sizeof(uint2));
+    off += ws_align(rows * 2 * cmax * (size_t)kTopKSlicePool * sizeof(uint2));
     return off;
 }
 
@@ -114,19 +120,18 @@ const DdExpTables &exp_tables() {
 }  // namespace
 
 extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V) {
-    (void)V;
-    if (B < 0 || n < 0) return 0;
+    if (B < 0 || n < 0 || V < 0) return 0;
     switch (kind) {
     case SPEC_WS_CHAIN:
     case SPEC_WS_CHAIN_TOPK: {
         const size_t rows = (size_t)B * ((size_t)n + 1);
-        return ws_layout_bytes(B, rows, chain_data_bytes(rows), nullptr, nullptr, kind == SPEC_WS_CHAIN_TOPK);
+        return ws_layout_bytes(B, rows, chain_data_bytes(rows), nullptr, nullptr, kind == SPEC_WS_CHAIN_TOPK, V);
     }
     case SPEC_WS_TREE:
         return ws_layout_bytes(B, 0, (size_t)B * (size_t)n * sizeof(unsigned long long), nullptr, nullptr,
                                false);
     case SPEC_WS_COMMIT:
-        return 2 * kWsHeader;
+        return kWsHeader + ws_align((size_t)B * sizeof(unsigned));
     default:
         return 0;
     }
@@ -158,7 +163,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         return SPEC_ERR_INVALID_ARG;
     const bool has_pool = ws_bytes >= spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, a->B, a->gamma, a->V);
     Ws w;
-    ws_layout_bytes(a->B, (size_t)rows, chain_data_bytes((size_t)rows), &w, workspace, has_pool);
+    ws_layout_bytes(a->B, (size_t)rows, chain_data_bytes((size_t)rows), &w, workspace, has_pool, a->V);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (greedy) {
@@ -213,21 +218,20 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.counters = w.counters;
         p.rejword = w.rejword;
         p.recs = static_cast<PosRec *>(w.data);
-        p.poscnt = w.poscnt;
-        p.poolcnt = w.poolcnt;
+        p.slicecb = w.slicecb;
         p.pool = w.pool;
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
         // top-k <= 128: cluster-free candidate lists when every slice's share
         // (about k + a few) fits the per-position pool; otherwise the cluster
         // kernel with its exact threshold search
-        const int cf = slices_for(a->V, a->dtype, 1 << 20, 32768);
+        const int cf = topk_slices(a->V, a->dtype);
         const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax &&
-                          (int64_t)cf * (p.top_k + 16) <= kTopKPool;
+                          (int64_t)cf * (p.top_k + 16) <= kTopKMerge;
         if (fast) {
             p.c = cf;
             p.Vs = slice_len(a->V, cf);
             if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
-            e = launch_chain_topk(p, a->dtype, s);
+            e = launch_chain_topk(p, a->dtype, sm_count(), s);
         } else {
             if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
             e = launch_chain_sample(p, a->dtype, s);
@@ -318,15 +322,14 @@ extern "C" int spec_commit_kv(const SpecCommitArgs *a, void *workspace, size_t w
     p.blocks_in_use = a->blocks_in_use;
     p.flags = a->flags;
     p.status = reinterpret_cast<unsigned *>(base);
-    p.counter = reinterpret_cast<unsigned *>(base + kWsHeader);
-    // enough warps to cover every SM a few times; the kernel strides over units
-    const int64_t max_units = (int64_t)a->B * a->S * a->L * 2;
-    const int warps_per_block = commit_threads() / 32;
-    int64_t grid = (max_units + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = (int64_t)sm_count() * 4;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    const cudaError_t e = launch_commit_kv(p, (int)grid, static_cast<cudaStream_t>(stream));
+    p.counters = reinterpret_cast<unsigned *>(base + kWsHeader);
+    const CommitGeom geo = commit_geometry(a->L, unit);
+    p.ppu = geo.ppu;
+    p.upp = geo.upp;
+    p.groups = geo.groups;
+    // one block per (request, slot, group); blocks past n_slots exit at once
+    if ((int64_t)a->B * a->S * p.groups > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_commit_kv(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 

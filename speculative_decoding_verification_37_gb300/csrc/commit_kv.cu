@@ -6,151 +6,152 @@
 // length advances; rejected slots are dropped by not advancing past them,
 // never by copying whole blocks.
 //
-// The work is a flat list of 2 KiB-class units (one token's K or V of one
-// layer: H*D elements).  Every block validates all requests (so a bad
-// request is skipped as a whole), builds the exclusive prefix of the
-// accepted token counts in shared memory, and then its warps copy units
-// unit = (layer*2 + kv) * tokens + token with 16-byte vector loads/stores.
-// Consecutive warps take consecutive tokens of one (layer, K|V), so source
-// and destination runs are contiguous within a request.  The last block to
-// finish (one arrival counter) advances the lengths; every other block only
-// reads them.
+// One single-warp block per (request b, accepted slot i, group): a group is
+// up to kCommitStage bytes of token i's 2*L units (one layer's K or V, H*D
+// elements each; units larger than a stage are split into pieces).  Lane 0
+// moves the group with the bulk-copy (TMA) engine: one cp.async.bulk per
+// unit from the temporary slots into shared memory, completing on one
+// mbarrier, then one bulk store per unit into the paged cache.  The bytes in
+// flight cost no registers, so many blocks share an SM.
+//
+// No prefix over the batch is needed: a block whose slot is past n_slots[b]
+// exits after one load.  The block's lanes validate the whole request (all
+// slots and block-table entries) in parallel, so a bad request is skipped as
+// a whole by every block.  The block that arrives last for a request (one
+// counter per request in the workspace) advances committed_len[b]; every
+// block of the request has read the old length before it arrives.
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace specv {
 
-constexpr int kCommitNT = 512;
-constexpr int kCommitBatch = 4;  // 16-byte chunks in flight per lane
+constexpr uint32_t kCommitStage = 16384;  // bytes one block moves
 
-int commit_threads() { return kCommitNT; }
-size_t commit_smem_bytes(int B) { return (size_t)(B + 1) * sizeof(int) + (size_t)B; }
-
-__global__ void __launch_bounds__(kCommitNT) commit_kv_kernel(CommitParams p) {
-    extern __shared__ int smem[];
-    int *prefix = smem;                                          // [B+1]
-    unsigned char *ok = reinterpret_cast<unsigned char *>(smem + p.B + 1);  // [B]
-    __shared__ int s_chunk[kCommitNT];
-    __shared__ int s_last;
-    const int B = p.B, tid = threadIdx.x;
-
-    // 1. validate each request; accepted count (0 if bad)
-    for (int b = tid; b < B; b += kCommitNT) {
-        const int n = p.n_slots[b];
-        const int len0 = p.len[b];
-        bool good = n >= 0 && n <= p.S && len0 >= 0 &&
-                    (int64_t)len0 + n <= (int64_t)p.max_blocks * p.bs;
-        for (int i = 0; good && i < n; ++i) {
-            const int s = p.slots ? p.slots[(int64_t)b * p.slots_stride + i] : i;
-            const int blk = p.table[(int64_t)b * p.max_blocks + (len0 + i) / p.bs];
-            good = s >= 0 && s < p.S && blk >= 0 && (int64_t)blk < p.nb;
-        }
-        ok[b] = good;
+CommitGeom commit_geometry(int L, int64_t unit_bytes) {
+    CommitGeom g;
+    if (unit_bytes > (int64_t)kCommitStage) {
+        g.ppu = (int)((unit_bytes + kCommitStage - 1) / kCommitStage);
+        g.upp = 1;
+        g.groups = 2 * L * g.ppu;
+    } else {
+        g.ppu = 1;
+        g.upp = (int)(kCommitStage / unit_bytes);
+        g.groups = (2 * L + g.upp - 1) / g.upp;
     }
-    __syncthreads();
-    // 2. exclusive prefix of the counts: contiguous chunk per thread, then a block scan
-    const int per = (B + kCommitNT - 1) / kCommitNT;
-    const int c0 = min(B, tid * per), c1 = min(B, c0 + per);
-    int sum = 0;
-    for (int b = c0; b < c1; ++b) sum += ok[b] ? p.n_slots[b] : 0;
-    s_chunk[tid] = sum;
-    __syncthreads();
-    if (tid < 32) {
-        // warp 0 scans the kCommitNT chunk totals
-        int carry = 0;
-        for (int base = 0; base < kCommitNT; base += 32) {
-            int v = s_chunk[base + tid];
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, incl, o);
-                if (tid >= o) incl += y;
-            }
-            s_chunk[base + tid] = carry + incl - v;
-            carry += __shfl_sync(kFull, incl, 31);
-        }
-        if (tid == 0) prefix[B] = carry;
-    }
-    __syncthreads();
-    {
-        int run = s_chunk[tid];
-        for (int b = c0; b < c1; ++b) {
-            prefix[b] = run;
-            run += ok[b] ? p.n_slots[b] : 0;
-        }
-    }
-    __syncthreads();
-
-    // 3. copy units
-    const int tokens = prefix[B];
-    const int64_t units = (int64_t)tokens * p.L * 2;
-    const int chunks = p.unit_bytes / 16;
-    const int lane = tid & 31;
-    const int64_t warp = (int64_t)blockIdx.x * (kCommitNT / 32) + (tid >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kCommitNT / 32);
-    for (int64_t u = warp; u < units; u += nwarps) {
-        const int lk = (int)(u / tokens);
-        const int t = (int)(u - (int64_t)lk * tokens);
-        // request of token t: the last b with prefix[b] <= t (empty requests skipped)
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        const int b = lo, i = t - prefix[b];
-        const int s = p.slots ? p.slots[(int64_t)b * p.slots_stride + i] : i;
-        const int pos = p.len[b] + i;
-        const int blk = p.table[(int64_t)b * p.max_blocks + pos / p.bs];
-        const int layer = lk >> 1, kv = lk & 1;
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            p.temp + ((((int64_t)b * p.L + layer) * 2 + kv) * p.S + s) * p.unit_bytes);
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            p.cache + ((((int64_t)layer * 2 + kv) * p.nb + blk) * p.bs + pos % p.bs) * p.unit_bytes);
-        for (int cb = lane; cb < chunks; cb += 32 * kCommitBatch) {
-            uint4 v[kCommitBatch];
-#pragma unroll
-            for (int q = 0; q < kCommitBatch; ++q)
-                if (cb + 32 * q < chunks) v[q] = ld_nc16(src + cb + 32 * q);
-#pragma unroll
-            for (int q = 0; q < kCommitBatch; ++q)
-                if (cb + 32 * q < chunks) dst[cb + 32 * q] = v[q];
-        }
-    }
-
-    // 4. the last block advances the lengths
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    unsigned any_bad = 0;
-    for (int b = tid; b < B; b += kCommitNT) {
-        if (ok[b]) {
-            const int nl = p.len[b] + p.n_slots[b];
-            p.len[b] = nl;
-            if (p.blocks_in_use) p.blocks_in_use[b] = (nl + p.bs - 1) / p.bs;
-        } else {
-            any_bad = 1;
-            if (p.flags) p.flags[b] |= SPEC_FLAG_BAD_INPUT;
-            if (p.blocks_in_use) p.blocks_in_use[b] = (p.len[b] + p.bs - 1) / p.bs;
-        }
-    }
-    if (__syncthreads_or(any_bad) && tid == 0) atomicOr(p.status, SPEC_FLAG_BAD_INPUT);
-    if (tid == 0) *p.counter = 0u;
+    return g;
 }
 
-cudaError_t launch_commit_kv(const CommitParams &p, int grid, cudaStream_t s) {
-    const size_t smem = commit_smem_bytes(p.B);
-    if (smem > 48 * 1024) {
-        // the largest B (32768) needs the most; set that once per device
-        static std::atomic<unsigned long long> done{0};
-        cudaError_t e = ensure_smem_attr(commit_kv_kernel, (int)commit_smem_bytes(32768), done);
-        if (e != cudaSuccess) return e;
+__global__ void __launch_bounds__(32) commit_kv_kernel(CommitParams p) {
+    __shared__ __align__(128) unsigned char stage[kCommitStage];
+    __shared__ __align__(8) unsigned long long bar;
+    const int lane = threadIdx.x;
+    const int G = p.groups, S = p.S;
+    const int64_t bi = blockIdx.x / G;
+    const int grp = (int)(blockIdx.x - bi * G);
+    const int b = (int)(bi / S), i = (int)(bi - (int64_t)b * S);
+    const bool head = i == 0 && grp == 0;
+
+    const int n = p.n_slots[b];
+    if (!head && (unsigned)i >= (unsigned)n) return;  // past n_slots (or n < 0: the head flags it)
+    const int len0 = p.len[b];
+    bool good = n >= 0 && n <= S && len0 >= 0 && (int64_t)len0 + n <= (int64_t)p.max_blocks * p.bs;
+    bool lane_ok = true;
+    int slot_i = 0, blk_i = 0;
+    if (good) {
+        for (int q = lane; q < n; q += 32) {
+            const int s = p.slots ? p.slots[(int64_t)b * p.slots_stride + q] : q;
+            const int blk = p.table[(int64_t)b * p.max_blocks + (len0 + q) / p.bs];
+            lane_ok = lane_ok && s >= 0 && s < S && blk >= 0 && (int64_t)blk < p.nb;
+            if (q == i) {
+                slot_i = s;
+                blk_i = blk;
+            }
+        }
     }
-    commit_kv_kernel<<<grid, kCommitNT, smem, s>>>(p);
+    good = __all_sync(kFull, lane_ok) && good;
+    slot_i = __shfl_sync(kFull, slot_i, i & 31);
+    blk_i = __shfl_sync(kFull, blk_i, i & 31);
+    if (lane != 0) return;
+    if (!good) {
+        if (head) {
+            if (p.flags) p.flags[b] |= SPEC_FLAG_BAD_INPUT;
+            if (p.blocks_in_use) p.blocks_in_use[b] = (len0 + p.bs - 1) / p.bs;
+            atomicOr(p.status, SPEC_FLAG_BAD_INPUT);
+        }
+        return;
+    }
+    if (n == 0) {
+        if (p.blocks_in_use) p.blocks_in_use[b] = (len0 + p.bs - 1) / p.bs;  // head only
+        return;
+    }
+
+    // pieces [k0, k1) of the token in (unit, piece) order
+    const int two_l = 2 * p.L;
+    const int64_t unit = p.unit_bytes;
+    const int k0 = grp * p.upp;
+    const int k1 = p.ppu > 1 ? k0 + 1 : min(two_l, k0 + p.upp);
+    auto piece = [&](int k, int &lk, int64_t &off, uint32_t &bytes) {
+        lk = k / p.ppu;
+        const int sub = k - lk * p.ppu;
+        off = (int64_t)sub * kCommitStage;
+        bytes = (uint32_t)min((int64_t)kCommitStage, unit - off);
+    };
+    const int pos = len0 + i;
+    const char *src_tok = p.temp + ((int64_t)b * two_l * S + slot_i) * unit;  // + lk*S*unit
+    char *dst_tok = p.cache + ((int64_t)blk_i * p.bs + pos % p.bs) * unit;    // + lk*nb*bs*unit
+    const int64_t dst_lk = p.nb * p.bs * unit;
+
+    uint32_t total = 0;
+    for (int k = k0; k < k1; ++k) {
+        int lk; int64_t off; uint32_t bytes;
+        piece(k, lk, off, bytes);
+        total += bytes;
+    }
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, total);
+    uint32_t so = 0;
+    for (int k = k0; k < k1; ++k) {
+        int lk; int64_t off; uint32_t bytes;
+        piece(k, lk, off, bytes);
+        bulk_g2s(stage + so, src_tok + (int64_t)lk * S * unit + off, bytes, &bar);
+        so += bytes;
+    }
+    bool ok = mbar_wait_bounded(&bar, 0u);
+    if (ok) {
+        so = 0;
+        for (int k = k0; k < k1; ++k) {
+            int lk; int64_t off; uint32_t bytes;
+            piece(k, lk, off, bytes);
+            bulk_s2g(dst_tok + lk * dst_lk + off, stage + so, bytes);
+            so += bytes;
+        }
+        bulk_commit();
+        bulk_wait_all();
+    } else {
+        // the loads are still outstanding: give them one more bounded wait
+        // before the block (and its shared memory) goes away
+        mbar_wait_bounded(&bar, 0u);
+        if (p.flags) atomicOr(p.flags + b, SPEC_FLAG_TIMEOUT);
+        atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+    }
+    mbar_inval(&bar);
+
+    // the last block of the request advances its length
+    __threadfence();
+    if (atomicAdd(p.counters + b, 1u) == (unsigned)(n * G - 1)) {
+        __threadfence();
+        const int nl = len0 + n;
+        p.len[b] = nl;
+        if (p.blocks_in_use) p.blocks_in_use[b] = (nl + p.bs - 1) / p.bs;
+        p.counters[b] = 0u;
+    }
+}
+
+cudaError_t launch_commit_kv(const CommitParams &p, cudaStream_t s) {
+    const int64_t grid = (int64_t)p.B * p.S * p.groups;
+    commit_kv_kernel<<<(unsigned)grid, 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

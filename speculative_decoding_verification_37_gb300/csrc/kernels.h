@@ -64,28 +64,35 @@ struct SampleParams {
     unsigned *status, *counters;
     unsigned *rejword;  // [B] earliest rejection seen: gamma - k + 1, 0 = none
     PosRec *recs;       // [B*(gamma+1)]
-    unsigned *poscnt;   // [B*(gamma+1)] top-k path: slices arrived per position
-    unsigned *poolcnt;  // [B*(gamma+1)][2] top-k path: candidates appended per row
-    uint2 *pool;        // [B*(gamma+1)][2][kTopKPool] top-k path: candidate (key, token)
+    // top-k path: per (position, row, slice) the candidate count with the
+    // bound's order key, and a region of kTopKSlicePool (order key, token id)
+    // entries, slice stride c
+    uint2 *slicecb;      // [B*(gamma+1)][2][c]
+    uint2 *pool;         // [B*(gamma+1)][2][c][kTopKSlicePool]
 };
 
-constexpr int kTopKPool = 2048;   // candidate entries per row per position (top-k path)
+constexpr int kTopKSlicePool = 256;  // candidates one slice of one row may hand on
+constexpr int kTopKMerge = 4096;     // candidates per row one position can merge
 
 struct CommitParams {
     int B, L, S, bs, unit_bytes, max_blocks, slots_stride;
+    int ppu, upp, groups;  // pieces per unit, units per group, groups per token
     const char *temp;
     char *cache;
     int64_t nb;
     const int *table, *slots, *n_slots;
     int *len, *blocks_in_use;
-    unsigned *flags, *status, *counter;
+    unsigned *flags, *status, *counters;  // counters: one per request, zero between calls
 };
 
 cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, cudaStream_t s);
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_chain_topk(const SampleParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_commit_kv(const CommitParams &p, int grid, cudaStream_t s);
-int commit_threads();
-size_t commit_smem_bytes(int B);
+cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s);
+int topk_row_bytes();  // a top-k slice body per row must fit this
+struct CommitGeom {
+    int ppu, upp, groups;
+};
+CommitGeom commit_geometry(int L, int64_t unit_bytes);
+cudaError_t launch_commit_kv(const CommitParams &p, cudaStream_t s);
 
 }  // namespace specv

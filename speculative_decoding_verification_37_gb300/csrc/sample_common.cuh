@@ -2,9 +2,10 @@
 //
 // verify_sample.cu runs one thread-block cluster per (position, request)
 // for full-vocabulary rows and for top-k rows whose threshold needs the
-// exact cluster-wide search; verify_topk.cu runs cluster-free blocks for
-// top-k rows.  Both end each position with masked_position() or
-// compact_position() below and finish() (record + request epilogue).
+// exact cluster-wide search; verify_topk.cu runs cluster-free kernels for
+// top-k rows.  Both end each position with finish() (record + request
+// epilogue); masked_position() below is the exact computation of one
+// position, over a cluster or over whole rows in one block.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -24,16 +25,12 @@ constexpr int kNW = kNT / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kSeg = 256;        // candidates one top-k slice may contribute per row
 constexpr int kScanE = 8;        // elements per thread per tile of the token-order scan
-constexpr int kKeptMax = 1024;   // kept (top-k) entries per row a position can sort
-constexpr int kPool = kTopKPool;  // top-k candidates per row a position can collect
+constexpr int kKeptMax = 256;    // kept (top-k) entries per row a position can sort
 
-// Dynamic shared memory: full-vocab rows stream through a ring; top-k rows
-// stage the whole slice pair, later reused for the merge.
+// Dynamic shared memory of the masked path: rows stream through a ring.
 constexpr int kRingCH = 8192, kRingNST = 4;
-constexpr int kFastStage = 32768;   // a top-k slice must fit in one stage per row
 using SampRing = Ring<kRingCH, kRingNST, 2>;
-using FastRing = Ring<kFastStage, 1, 2>;
-constexpr size_t kSampDyn = sizeof(SampRing) > sizeof(FastRing) ? sizeof(SampRing) : sizeof(FastRing);
+constexpr size_t kSampDyn = sizeof(SampRing);
 
 struct SampBase {
     float2 red2[kNW];
@@ -589,162 +586,6 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
         }
     }
     if (j == writer) finish(p, b, k, o, sb);
-}
-
-// ---------------------------------------------------------------------------
-// One top-k position from candidate lists already in shared memory: list r
-// (row 0 = target, 1 = draft) holds n[r] entries (order key, token id) that
-// include every logit >= the row's k-th largest.  The exact threshold comes
-// from a block select, the kept set is sorted by token id (so every later
-// sum runs in a fixed order), and acceptance, residual mass and the draw are
-// computed in double-float over the kept sets.  `work` is shared memory for
-// 3 * kKeptMax entries.  One CTA; it calls finish().  A kept set larger than
-// kKeptMax (massive ties) falls back to masked_position over the whole row
-// in this block (`solo` exchange; `dsm` is then its streaming ring).
-// ---------------------------------------------------------------------------
-template <typename T, typename Solo>
-__device__ void compact_position(const SampleParams &p, SampBase &sb, const uint2 *const *lists,
-                                 const int *n, uint2 *work, unsigned char *dsm, Solo &solo, int k,
-                                 int b) {
-    constexpr int KB = Elem<T>::KEY_BITS;
-    const int tid = threadIdx.x, g = p.gamma;
-    const bool has_draft = k < g;
-    const T *drow = has_draft
-        ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
-    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
-    const dd c2d{p.c2_hi, p.c2_lo};
-    const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
-    const bool bad_tok = has_draft && (d < 0 || d >= p.V);
-    const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
-    const float g_d = (has_draft && !bad_tok) ? ld_elem(drow, d) : 0.0f;
-    const float u_k = has_draft ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
-    const float u_f = p.unif[(int64_t)b * (g + 1) + g];
-    Outcome o{1.0f, 0.0f, -1, 0u};
-    const int rows = has_draft ? 2 : 1;
-    __shared__ int s_kn[2];
-    uint32_t th[2] = {0u, 0u};
-    unsigned kn[2] = {0u, 0u};
-    for (int r = 0; r < rows; ++r) {
-        const uint2 *L = lists[r];
-        const int nr = n[r];
-        th[r] = block_kth_largest<KB, kNT>(
-            [&](auto &&f) { for (int x = tid; x < nr; x += kNT) f(L[x].x); },
-            (unsigned)min(p.top_k, nr), sb.hist, sb.bc);
-        unsigned cnt = 0;
-        for (int x = tid; x < nr; x += kNT) cnt += L[x].x >= th[r];
-        kn[r] = block_sum_u<kNT>(cnt, sb.redu);
-    }
-    if (kn[0] > (unsigned)kKeptMax || kn[1] > (unsigned)kKeptMax) {
-        // hundreds of logits tied at the threshold: the exact masked path over
-        // the whole row in this one block
-        masked_position<T, true>(p, sb, dsm, solo, k, b, 0, p.V);
-        return;
-    }
-    uint2 *sorted[2] = {work, work + kKeptMax};
-    uint2 *tmp = work + 2 * kKeptMax;  // free until the draw
-    for (int r = 0; r < rows; ++r) {
-        // compact the kept entries, then place each at its rank in token order
-        // (rank = number of kept entries with a smaller id; ids are distinct)
-        const uint2 *L = lists[r];
-        const int nr = n[r];
-        if (tid == 0) s_kn[r] = 0;
-        __syncthreads();
-        for (int x = tid; x < nr; x += kNT) {
-            const uint2 e = L[x];
-            if (e.x >= th[r]) tmp[atomicAdd(&s_kn[r], 1)] = e;
-        }
-        __syncthreads();
-        const int m = (int)kn[r];
-        for (int x = tid; x < m; x += kNT) {
-            const uint2 e = tmp[x];
-            int rank = 0;
-            for (int y = 0; y < m; ++y) rank += tmp[y].y < e.y;
-            sorted[r][rank] = e;
-        }
-        __syncthreads();
-    }
-    // row statistics in dd over the kept sets (fixed order per thread)
-    const float2 *tab = sb.tab;
-    const float2 ln2 = sb.ln2;
-    const uint2 *Kp = sorted[0];
-    const uint2 *Kq = sorted[1];
-    const int np = s_kn[0], nq = rows == 2 ? s_kn[1] : 0;
-    float mp = -INFINITY, mq = -INFINITY;
-    for (int i = tid; i < np; i += kNT) mp = fmaxf(mp, key_value<T>(Kp[i].x));
-    for (int i = tid; i < nq; i += kNT) mq = fmaxf(mq, key_value<T>(Kq[i].x));
-    mp = block_ms<kNT>(MaxSum{mp, 0.0f}, 1.0f, sb.red2).m;
-    mq = block_ms<kNT>(MaxSum{mq, 0.0f}, 1.0f, sb.red2).m;
-    const bool bad_row = mp == -INFINITY || (has_draft && mq == -INFINITY);
-    dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f};
-    if (!bad_row) {
-        for (int i = tid; i < np; i += kNT) sp = dd_add(sp, dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2));
-        for (int i = tid; i < nq; i += kNT) sq = dd_add(sq, dd_expw(key_value<T>(Kq[i].x), mq, c2d, tab, ln2));
-    }
-    block_dd_sum2<kNT>(sp, sq, sb.redd);
-    const bool bad = bad_tok || bad_row;
-    o.info = (bad_tok ? REC_BAD_INPUT : 0u) | (bad_row ? REC_BAD_ROW : 0u);
-    if (!bad) {
-        const dd isp = dd_recip(sp);
-        const dd isq = has_draft ? dd_recip(sq) : dd{0.0f, 0.0f};
-        bool accept = false;
-        if (has_draft) {
-            const dd pd = kkey<T>(l_d) >= th[0] ? dd_mul(dd_expw(l_d, mp, c2d, tab, ln2), isp) : dd{0.0f, 0.0f};
-            const dd qd = kkey<T>(g_d) >= th[1] ? dd_mul(dd_expw(g_d, mq, c2d, tab, ln2), isq) : dd{0.0f, 0.0f};
-            float a;
-            if (dd_pos(qd)) {
-                const dd ratio = dd_mul(pd, dd_recip(qd));
-                a = dd_gt(ratio, dd{1.0f, 0.0f}) ? 1.0f : dd_to_f(ratio);
-            } else {
-                a = dd_pos(pd) ? 1.0f : 0.0f;
-            }
-            o.a = a;
-            accept = u_k < a;
-            o.info |= accept ? REC_ACCEPT : 0u;
-        }
-        // residual weights over the target's kept set (q gathered from the draft row)
-        auto qprob = [&](int idx) -> dd {
-            const float y = ld_elem(drow, idx);
-            return kkey<T>(y) >= th[1] ? dd_mul(dd_expw(y, mq, c2d, tab, ln2), isq) : dd{0.0f, 0.0f};
-        };
-        dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
-        if (has_draft) {
-            for (int i = tid; i < np; i += kNT) {
-                const dd pi = dd_mul(dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2), isp);
-                zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qprob((int)Kp[i].y)))));
-                zp = dd_add(zp, pi);
-            }
-            block_dd_sum2<kNT>(zw, zp, sb.redd);
-            o.z = dd_to_f(zw);
-        }
-        if (tid == 0) sb.rej = *((volatile unsigned *)&p.rejword[b]);
-        __syncthreads();
-        const bool earlier = sb.rej > (unsigned)(g - k + 1);
-        if (has_draft && !accept && tid == 0) atomicMax(p.rejword + b, (unsigned)(g - k + 1));
-        if ((!has_draft || !accept) && !earlier) {
-            // ---- the draw, in token order over the kept set ----
-            const bool fb = has_draft && dd_le(zw, dd{p.eps, 0.0f});
-            if (fb) o.info |= REC_FALLBACK;
-            const bool use_p = !has_draft || fb;
-            const dd total = !has_draft ? sp : (fb ? zp : zw);
-            const dd t = dd_mul_f(total, u_f);
-            // the kept set is already in token order
-            float2 *ws = reinterpret_cast<float2 *>(work + 2 * kKeptMax);
-            __syncthreads();
-            for (int i = tid; i < np; i += kNT) {
-                dd wgt = dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2);
-                if (has_draft) {
-                    wgt = dd_mul(wgt, isp);
-                    if (!use_p) wgt = dd_max0(dd_add(wgt, dd_neg(qprob((int)Kp[i].y))));
-                }
-                ws[i] = make_float2(wgt.hi, wgt.lo);
-            }
-            __syncthreads();
-            o.token = dd_scan_slice<kNT>(0, np, dd{0.0f, 0.0f}, t,
-                                         [&](int i) { return dd{ws[i].x, ws[i].y}; }, sb);
-            if (o.token >= 0) o.token = (int)Kp[o.token].y;
-        }
-    }
-    finish(p, b, k, o, sb);
 }
 
 }  // namespace specv

@@ -70,6 +70,19 @@ __device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t 
         : "memory");
 }
 
+// bulk copy of `bytes` from shared to global memory (same alignment rules),
+// tracked by the issuing thread's bulk async-group
+__device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// waits until every committed bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Ring of NST stages x ROWS rows x CH bytes.
 template <int CH, int NST, int ROWS> struct Ring {
     alignas(128) unsigned char buf[NST][ROWS][CH];

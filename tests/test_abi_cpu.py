@@ -77,7 +77,7 @@ def test_struct_layouts_match_c(lib):
 def test_workspace_sizes(lib):
     assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN, 64, 4, 128256) >= 256 + 64 * 4 + 64 * 5 * 16
     assert L.spec_workspace_bytes(L.SPEC_WS_TREE, 128, 5, 128256) >= 256 + 128 * 4 + 128 * 5 * 8
-    assert L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 512, 0, 0) >= 512
+    assert L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 512, 0, 0) >= 256 + 512 * 4
     base = L.spec_workspace_bytes(L.SPEC_WS_CHAIN, 64, 4, 128256)
     assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 64, 4, 128256) >= base + 64 * 5 * 2 * 2048 * 8
     assert L.spec_workspace_bytes(99, 1, 1, 1) == 0

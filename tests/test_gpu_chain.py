@@ -66,6 +66,23 @@ def test_sampled_chain_misaligned_strided_rows(dt):
     compare_chain(batch, gpu, range(B))
 
 
+@pytest.mark.parametrize("dt,layout", [("bf16", "same-phase"), ("f32", "same-phase"),
+                                       ("bf16", "phase-mismatch"), ("f32", "phase-mismatch")])
+def test_sampled_topk_strided_rows(dt, layout):
+    """Top-k rows inside wider buffers: equal 16-byte phases take the bulk
+    copies plus scalar heads and tails; unequal phases take the exact path."""
+    B, g, V, k = 4, 3, 9001, 20
+    batch = W.make_chain(spec(B, g, V, dt, 0.9, k), seed=23)
+    width = 9016  # a multiple of 8 elements: every row starts at the same phase
+    ot, od = (3, 3) if layout == "same-phase" else (3, 6)
+    tgt = torch.zeros((B * (g + 1), width), dtype=batch.target.dtype)
+    drf = torch.zeros((B * g, width), dtype=batch.draft.dtype)
+    tgt[:, ot:ot + V] = batch.target
+    drf[:, od:od + V] = batch.draft
+    gpu = run_chain(batch, target=tgt.cuda()[:, ot:ot + V], draft=drf.cuda()[:, od:od + V])
+    compare_chain(batch, gpu, range(B))
+
+
 @pytest.mark.parametrize("dt,k", [("bf16", 5), ("f32", 3), ("bf16", 40)])
 def test_sampled_topk_with_heavy_ties(dt, k):
     """Logits on a coarse grid: many ties at the k-th value, all kept."""
