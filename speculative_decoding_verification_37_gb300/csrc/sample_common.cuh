@@ -273,44 +273,79 @@ __device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBas
 }
 
 // ---------------------------------------------------------------------------
-// The request epilogue: the last position to arrive writes the outputs.
+// The request epilogue: the last position to arrive writes the outputs.  Run
+// by one warp: lane q reads position q's record (one L2 load each, all in
+// flight together), ballots find the first rejection and any bad input.
 // ---------------------------------------------------------------------------
-static __device__ void write_request(const SampleParams &p, int b) {
-    const int g = p.gamma;
-    __threadfence();
-    const volatile PosRec *R = p.recs + (int64_t)b * (g + 1);
-    unsigned badbits = 0;
-    for (int q = 0; q <= g; ++q) {
-        const unsigned info = R[q].info;
-        badbits |= (info & REC_BAD_INPUT) ? SPEC_FLAG_BAD_INPUT : 0u;
-        badbits |= (info & REC_BAD_ROW) ? SPEC_FLAG_BAD_ROW : 0u;
-    }
-    if (badbits) {
-        p.n_acc[b] = 0;
-        p.n_out[b] = 0;
-        if (p.flags) p.flags[b] = badbits;
-        atomicOr(p.status, badbits);
-    } else {
-        int n = g;
-        for (int q = 0; q < g; ++q)
-            if (!(R[q].info & REC_ACCEPT)) { n = q; break; }
-        int *out = p.out_tokens + (int64_t)b * (g + 1);
-        const int *dt = p.tokens + (int64_t)b * g;
-        for (int q = 0; q < n; ++q) out[q] = dt[q];
-        out[n] = R[n].token;
-        p.n_acc[b] = n;
-        p.n_out[b] = n + 1;
-        if (p.accept_prob)
-            for (int q = 0; q < g; ++q) p.accept_prob[(int64_t)b * g + q] = R[q].a;
-        if (p.resid)
-            for (int q = 0; q < g; ++q) p.resid[(int64_t)b * g + q] = R[q].z;
-        if (p.flags) p.flags[b] = (R[n].info & REC_FALLBACK) ? SPEC_FLAG_FALLBACK : 0u;
-    }
-    p.rejword[b] = 0u;
-    p.counters[b] = 0u;
+__device__ __forceinline__ PosRec load_rec(const PosRec *r) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(r));
+    PosRec x;
+    x.a = __uint_as_float(v.x);
+    x.z = __uint_as_float(v.y);
+    x.token = (int)v.z;
+    x.info = v.w;
+    return x;
 }
 
+static __device__ void write_request_warp(const SampleParams &p, int b) {
+    const int g = p.gamma, lane = threadIdx.x & 31;
+    __threadfence();
+    const PosRec *R = p.recs + (int64_t)b * (g + 1);
+    unsigned badbits = 0;
+    int n = g;  // the first rejecting position (g: all accepted)
+    PosRec mine{};
+    for (int q0 = 0; q0 <= g; q0 += 32) {
+        const int q = q0 + lane;
+        PosRec r{};
+        if (q <= g) r = load_rec(R + q);
+        if (q0 == 0) mine = r;
+        badbits |= (q <= g && (r.info & REC_BAD_INPUT)) ? SPEC_FLAG_BAD_INPUT : 0u;
+        badbits |= (q <= g && (r.info & REC_BAD_ROW)) ? SPEC_FLAG_BAD_ROW : 0u;
+        const unsigned rej = __ballot_sync(kFull, q < g && !(r.info & REC_ACCEPT));
+        if (n == g && rej) n = q0 + __ffs(rej) - 1;
+    }
+    badbits = __reduce_or_sync(kFull, badbits);
+    if (badbits) {
+        if (lane == 0) {
+            p.n_acc[b] = 0;
+            p.n_out[b] = 0;
+            if (p.flags) p.flags[b] = badbits;
+            atomicOr(p.status, badbits);
+        }
+    } else {
+        int *out = p.out_tokens + (int64_t)b * (g + 1);
+        const int *dt = p.tokens + (int64_t)b * g;
+        for (int q0 = 0; q0 <= g; q0 += 32) {
+            const int q = q0 + lane;
+            if (q > g) break;
+            const PosRec r = q0 == 0 ? mine : load_rec(R + q);
+            if (q < n) out[q] = dt[q];
+            if (q == n) {
+                out[n] = r.token;
+                if (p.flags) p.flags[b] = (r.info & REC_FALLBACK) ? SPEC_FLAG_FALLBACK : 0u;
+            }
+            if (q < g) {
+                if (p.accept_prob) p.accept_prob[(int64_t)b * g + q] = r.a;
+                if (p.resid) p.resid[(int64_t)b * g + q] = r.z;
+            }
+        }
+        if (lane == 0) {
+            p.n_acc[b] = n;
+            p.n_out[b] = n + 1;
+        }
+    }
+    if (lane == 0) {
+        p.rejword[b] = 0u;
+        p.counters[b] = 0u;
+    }
+}
+
+// Records position k's outcome; the position that arrives last for request b
+// writes the request's outputs.  Called by every thread of the block (or, in
+// a warp-only caller, every lane of warp 0); warp 0 does the work.
 static __device__ void finish(const SampleParams &p, int b, int k, const Outcome &o, SampBase &sb) {
+    if (threadIdx.x >= 32) return;
+    unsigned last = 0u;
     if (threadIdx.x == 0) {
         PosRec rec;
         rec.a = o.a;
@@ -319,11 +354,11 @@ static __device__ void finish(const SampleParams &p, int b, int k, const Outcome
         rec.info = o.info;
         p.recs[(int64_t)b * (p.gamma + 1) + k] = rec;
         __threadfence();
-        sb.arrive_last = atomicAdd(p.counters + b, 1u) == (unsigned)p.gamma;
-        if (sb.arrive_last) write_request(p, b);
+        last = atomicAdd(p.counters + b, 1u) == (unsigned)p.gamma;
     }
+    if (__shfl_sync(kFull, last, 0)) write_request_warp(p, b);
+    (void)sb;
 }
-
 
 // ---------------------------------------------------------------------------
 // Exchange between the CTAs that share one position: a real thread-block

@@ -70,6 +70,24 @@ __device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t 
         : "memory");
 }
 
+// L2 policy for data read once: its lines are the first to go, so a stream
+// of logits does not push out the small results written next to it
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// bulk_g2s with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s_policy(void *sdst, const void *gsrc, uint32_t bytes,
+                                                unsigned long long *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // bulk copy of `bytes` from shared to global memory (same alignment rules),
 // tracked by the issuing thread's bulk async-group
 __device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {

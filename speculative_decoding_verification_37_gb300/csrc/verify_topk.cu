@@ -112,8 +112,11 @@ __device__ __forceinline__ void tk_issue(const SampleParams &p, TkRing &R, unsig
     const uint32_t nb = it.ok ? (uint32_t)((it.sp.tail0 - it.sp.body0) * (int)sizeof(T)) : 0u;
     mbar_arrive_expect_tx(&full[s], nb * (uint32_t)it.rows);
     if (nb) {
-        bulk_g2s(R.buf[s][0], it.trow + it.sp.body0, nb, &full[s]);
-        if (it.rows == 2) bulk_g2s(R.buf[s][1], it.drow + it.sp.body0, nb, &full[s]);
+        // the logits are read once: evict them first, keeping the candidate
+        // regions in L2 for the merge
+        const uint64_t pol = l2_evict_first();
+        bulk_g2s_policy(R.buf[s][0], it.trow + it.sp.body0, nb, &full[s], pol);
+        if (it.rows == 2) bulk_g2s_policy(R.buf[s][1], it.drow + it.sp.body0, nb, &full[s], pol);
     }
 }
 // largest element of a 16-byte vector (bf16: packed maxima)
@@ -581,23 +584,31 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
                     e[q] = __ldcg(&p.pool[tk_region(p, pos, r, lo) * kTopKSlicePool + (fr - s_off[r][lo])]);
                 }
             }
+            // keep masks per row, then one shared-memory atomic per warp and row
+            uint32_t km[2] = {0u, 0u};
 #pragma unroll
             for (int q = 0; q < BATCH; ++q) {
                 const unsigned f = f0 + q * kNT + tid;
                 const int r = f >= n0;
-                const bool keep = f < ntot && e[q].x >= s_tstar[r];
-                // one warp's entries may span both rows: aggregate per row
+                if (f < ntot && e[q].x >= s_tstar[r]) km[r] |= 1u << q;
+            }
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const bool kr = keep && r == rr;
-                    const unsigned bal = __ballot_sync(kFull, kr);
-                    if (bal) {
-                        int base = 0;
-                        if (lane == 0) base = atomicAdd(&s_n[rr], __popc(bal));
-                        base = __shfl_sync(kFull, base, 0) + __popc(bal & lt);
-                        if (kr) lists[rr * kTopKMerge + base] = e[q];
-                    }
+            for (int rr = 0; rr < 2; ++rr) {
+                const unsigned cnt = __popc(km[rr]);
+                unsigned incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
                 }
+                const unsigned wtot = __shfl_sync(kFull, incl, 31);
+                if (wtot == 0u) continue;
+                unsigned base = 0u;
+                if (lane == 31) base = (unsigned)atomicAdd(&s_n[rr], (int)wtot);
+                base = __shfl_sync(kFull, base, 31) + incl - cnt;
+#pragma unroll
+                for (int q = 0; q < BATCH; ++q)
+                    if (km[rr] & (1u << q)) lists[rr * kTopKMerge + base++] = e[q];
             }
         }
         __syncthreads();
@@ -770,7 +781,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
             o.token = sel >= 0 ? (int)Kp[sel].y : -1;
         }
     }
-    if (lane == 0) finish(p, b, k, o, sb);
+    finish(p, b, k, o, sb);
 }
 
 static_assert(2 * kTopKMerge * sizeof(uint2) <= kSampDyn, "the merged lists fit the fallback ring's memory");
