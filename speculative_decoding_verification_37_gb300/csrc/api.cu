@@ -99,9 +99,10 @@ size_t chain_data_bytes(size_t rows) {
     return rec > keys ? rec : keys;
 }
 
-// Double-float constants for the on-device exp2: ln 2 and 2^(j/64), j = -32..32,
-// each value computed in double on the host and split as hi = (float)v,
-// lo = (float)(v - hi).
+// Double-float constants for the on-device exponential: ln2/64 in three
+// parts (the first rounded to 11 significant bits) and 2^(j/64), j = 0..63,
+// each computed in double on the host and split as hi = (float)v,
+// lo = (float)(v - hi).  1/T is filled in per call.
 void split(double v, float2 &out) {
     out.x = (float)v;
     out.y = (float)(v - (double)out.x);
@@ -110,8 +111,16 @@ void split(double v, float2 &out) {
 const DdExpTables &exp_tables() {
     static const DdExpTables t = [] {
         DdExpTables x;
-        split(0.69314718055994530942, x.ln2);
-        for (int j = -32; j <= 32; ++j) split(std::exp2((double)j / 64.0), x.tab[j + 32]);
+        const long double c = 0.693147180559945309417232121458176568L / 64.0L;
+        int ex;
+        std::frexp((double)c, &ex);
+        const double q = std::ldexp(1.0, ex - 11);  // 11 significant bits
+        const double c1 = std::nearbyint((double)c / q) * q;
+        x.c1 = (float)c1;
+        x.c2 = (float)(c - (long double)x.c1);
+        x.c3 = (float)(c - (long double)x.c1 - (long double)x.c2);
+        for (int j = 0; j < 64; ++j) split(std::exp2((double)j / 64.0), x.tab[j]);
+        x.it = make_float2(1.0f, 0.0f);
         return x;
     }();
     return t;
@@ -201,11 +210,8 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.unif = a->uniforms;
         const double c2 = 1.4426950408889634074 / (double)a->temperature;
         p.c2 = (float)c2;
-        float2 c2s;
-        split(c2, c2s);
-        p.c2_hi = c2s.x;
-        p.c2_lo = c2s.y;
         p.exptab = exp_tables();
+        split(1.0 / (double)a->temperature, p.exptab.it);
         p.top_k = (a->top_k >= a->V) ? 0 : a->top_k;
         p.eps = a->fallback_eps;
         p.n_acc = a->n_acc;

@@ -4,12 +4,15 @@
 // is taken at close to float64 precision without the GB300's slow FP64 path.
 //
 // Error-free transformations: Knuth's TwoSum, Dekker's Fast2Sum and the
-// FMA-based TwoProd (Dekker 1971; Knuth, TAOCP vol. 2, 4.2.2).  exp2 follows
-// Tang's table-driven reduction (Tang 1989, ACM TOMS 15(2)):
-//   2^y = 2^n * 2^(j/64) * e^(r ln 2),  n = rint(y), j = rint(64 (y - n)),
-//   |r| <= 1/128, with e^z = 1 + z + z^2/2 + z^3/6 + z^4/24 + z^5/120
-//   (the next term is below 4e-17 for |z| <= 0.0055).  The 2^(j/64) values
-//   and ln 2 come from the host in double and are split into dd pairs.
+// FMA-based TwoProd (Dekker 1971; Knuth, TAOCP vol. 2, 4.2.2).  The
+// exponential follows Tang's table-driven method (Tang 1989, ACM TOMS
+// 15(2)) in base e with a Cody-Waite reduction (Cody and Waite 1980):
+//   y = k ln2/64 + s,  |s| <= ln2/128,  e^y = 2^(k>>6) * 2^((k&63)/64) * e^s,
+//   e^s = 1 + s + s^2/2 + s^3/6 + s^4/24 + s^5/120 (the next term is below
+//   4e-17).  ln2/64 is held in three parts, the first with 11 significant
+//   bits, so that k*c1 is exact for |k| < 2^13 and y - k*c1 is exact
+//   (Sterbenz); the 2^(j/64) values come from the host in double and are
+//   split into dd pairs.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -79,38 +82,55 @@ __device__ __forceinline__ bool dd_pos(dd a) { return a.hi > 0.0f || (a.hi == 0.
 __device__ __forceinline__ dd dd_max0(dd a) { return dd_pos(a) ? a : dd{0.0f, 0.0f}; }
 __device__ __forceinline__ float dd_to_f(dd a) { return __fadd_rn(a.hi, a.lo); }
 
-// Constants a kernel needs for dd exp2: ln 2 and 2^(j/64), j = -32..32.
-struct DdExpTables {
-    float2 ln2;          // (hi, lo)
-    float2 tab[65];      // 2^((j-32)/64) as (hi, lo)
-};
-
-// 2^y for y <= 0 (values below 2^-125 flush to 0, far below any tolerance here).
-__device__ __forceinline__ dd dd_exp2(dd y, const float2 *tab, float2 ln2) {
-    const float n = rintf(y.hi);
-    if (n < -125.0f) return dd{0.0f, 0.0f};
-    const dd f = fast_two_sum(__fsub_rn(y.hi, n), y.lo);   // y.hi - n is exact
-    const float jf = rintf(__fmul_rn(f.hi, 64.0f));
-    const dd r = fast_two_sum(__fsub_rn(f.hi, __fmul_rn(jf, 0.015625f)), f.lo);  // exact subtraction
-    const dd z = dd_mul(r, dd{ln2.x, ln2.y});
-    const dd z2 = dd_mul(z, z);
-    const float zh = z.hi;
-    const float tail = __fmul_rn(__fmul_rn(zh, __fmul_rn(zh, zh)),
-                                 __fmaf_rn(zh, __fmaf_rn(zh, 1.0f / 120.0f, 1.0f / 24.0f), 1.0f / 6.0f));
-    dd s = dd_add_f(z, 1.0f);
-    s = dd_add(s, dd{__fmul_rn(z2.hi, 0.5f), __fmul_rn(z2.lo, 0.5f)});
-    s = dd_add_f(s, tail);
-    const float2 t = tab[(int)jf + 32];
-    s = dd_mul(s, dd{t.x, t.y});
-    const float scale = __int_as_float(((int)n + 127) << 23);  // 2^n, exact for n >= -126
-    return dd{__fmul_rn(s.hi, scale), __fmul_rn(s.lo, scale)};
+// acc + v for non-negative terms: TwoSum on the high parts, the low parts
+// added in fp32, then renormalised (Dekker's add; relative error ~2^-45 for
+// terms of one sign).  Cheaper than dd_add, which also serves mixed signs.
+__device__ __forceinline__ dd dd_acc(dd acc, dd v) {
+    const dd s = two_sum(acc.hi, v.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(acc.lo, v.lo)));
 }
 
-// e^((x - m)/T) = 2^((x - m) * c2) with c2 = log2(e)/T given as a dd pair.
-__device__ __forceinline__ dd dd_expw(float x, float m, dd c2, const float2 *tab, float2 ln2) {
-    if (x == -INFINITY) return dd{0.0f, 0.0f};
-    const dd d = two_sum(x, -m);
-    return dd_exp2(dd_mul(d, c2), tab, ln2);
+// Constants of the double-float exponential: 1/T as a dd pair, ln2/64 in
+// three parts, and 2^(j/64), j = 0..63, as dd pairs.
+struct DdExpTables {
+    float2 it;           // 1 / temperature, (hi, lo)
+    float c1, c2, c3;    // ln2/64 = c1 + c2 + c3, c1 with 11 significant bits
+    float2 tab[64];      // 2^(j/64) as (hi, lo)
+};
+
+// e^((x - m)/T) for x <= m: a dd pair with relative error below ~1e-13 where
+// (x - m)/T > -30 (the terms that carry probability mass); values below
+// e^-86.6 flush to 0, -inf gives 0.
+__device__ __forceinline__ dd dd_expw(float x, float m, const DdExpTables &K) {
+    if (!(x > -INFINITY)) return dd{0.0f, 0.0f};
+    const dd d = two_sum(x, -m);  // exact
+    // y = d / T as an unnormalised pair (yh, yl)
+    const float yh = __fmul_rn(d.hi, K.it.x);
+    const float yl = __fadd_rn(__fmaf_rn(d.hi, K.it.x, -yh),
+                               __fmaf_rn(d.hi, K.it.y, __fmul_rn(d.lo, K.it.x)));
+    const float kf = rintf(__fmul_rn(yh, 92.332482616893657f));  // 64 / ln 2
+    if (kf < -8000.0f) return dd{0.0f, 0.0f};
+    // s = y - k ln2/64 as a dd pair
+    const float s1 = __fmaf_rn(-kf, K.c1, yh);  // exact
+    const dd t2 = two_prod(kf, K.c2);
+    dd s = two_sum(s1, -t2.hi);
+    s = dd_add_f(s, yl);
+    s.lo = __fadd_rn(s.lo, -__fmaf_rn(kf, K.c3, t2.lo));
+    // e^s: 1 + h + h^2/2 exactly, the rest in fp32
+    const float h = s.hi;
+    const dd sq = two_prod(h, h);
+    const float cub = __fmul_rn(__fmul_rn(h, sq.hi),
+                                __fmaf_rn(h, __fmaf_rn(h, 1.0f / 120.0f, 1.0f / 24.0f), 1.0f / 6.0f));
+    const float tail = __fadd_rn(__fadd_rn(s.lo, __fmul_rn(h, s.lo)), __fmaf_rn(0.5f, sq.lo, cub));
+    const dd e1 = fast_two_sum(1.0f, h);
+    const dd e2 = fast_two_sum(e1.hi, __fmul_rn(0.5f, sq.hi));
+    dd e = fast_two_sum(e2.hi, __fadd_rn(__fadd_rn(e1.lo, e2.lo), tail));
+    // times 2^(k/64)
+    const int ki = (int)kf;
+    const float2 t = K.tab[ki & 63];
+    e = dd_mul(e, dd{t.x, t.y});
+    const float scale = __int_as_float(((ki >> 6) + 127) << 23);  // 2^(k>>6), k>>6 >= -125
+    return dd{__fmul_rn(e.hi, scale), __fmul_rn(e.lo, scale)};
 }
 
 // warp-level dd sum in a fixed butterfly order (every lane gets the result)

@@ -54,8 +54,7 @@ struct SampleParams {
     const int *tokens;
     const float *unif;
     float c2;      // log2(e) / temperature
-    float c2_hi, c2_lo;   // the same as a double-float pair
-    DdExpTables exptab;   // ln 2 and 2^(j/64) as double-float pairs
+    DdExpTables exptab;   // 1/T, ln2/64 in parts, 2^(j/64): the double-float exponential
     int top_k;     // 0 = keep all
     float eps;
     int *n_acc, *out_tokens, *n_out;

@@ -47,9 +47,18 @@ struct SampBase {
     unsigned hist[256];
     unsigned bc[2];
     unsigned tau[2];
-    float2 tab[65];
-    float2 ln2;
+    DdExpTables K;                // the double-float exponential's constants
 };
+
+// copies the exponential's constants into shared memory (every thread calls;
+// a block barrier must follow before use)
+__device__ __forceinline__ void load_exp_tables(const SampleParams &p, SampBase &sb) {
+    constexpr int W = (int)(sizeof(DdExpTables) / sizeof(uint32_t));
+    static_assert(sizeof(DdExpTables) % sizeof(uint32_t) == 0, "word copy");
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(&p.exptab);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&sb.K);
+    for (int i = threadIdx.x; i < W; i += blockDim.x) dst[i] = src[i];
+}
 
 struct Outcome {
     float a, z;
@@ -408,7 +417,6 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     const T *drow = has_draft
         ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
     const float c2 = p.c2;
-    const dd c2d{p.c2_hi, p.c2_lo};
     const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
     const bool bad_tok = has_draft && (d < 0 || d >= p.V);
     const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
@@ -524,14 +532,13 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
 
     if (draw) {
         // ---- the draw in dd: slice sums (pass A), residual (pass B), scan ----
-        const float2 *tab = sb.tab;
-        const float2 ln2 = sb.ln2;
+        const DdExpTables &K = sb.K;
         const float mp = Mp.m, mq = Mq.m;
         auto ep = [&](float x) -> dd {
-            return (!MASK || (fkey(x) >> KS) >= th_p) ? dd_expw(x, mp, c2d, tab, ln2) : dd{0.0f, 0.0f};
+            return (!MASK || (fkey(x) >> KS) >= th_p) ? dd_expw(x, mp, K) : dd{0.0f, 0.0f};
         };
         auto eq = [&](float y) -> dd {
-            return (!MASK || (fkey(y) >> KS) >= th_q) ? dd_expw(y, mq, c2d, tab, ln2) : dd{0.0f, 0.0f};
+            return (!MASK || (fkey(y) >> KS) >= th_q) ? dd_expw(y, mq, K) : dd{0.0f, 0.0f};
         };
         dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f};
         if (has_draft) {

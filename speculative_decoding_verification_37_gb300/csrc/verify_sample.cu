@@ -40,8 +40,7 @@ __global__ void __launch_bounds__(kNT) chain_sample_kernel(SampleParams p) {
     __shared__ SampBase sb;
     extern __shared__ __align__(128) unsigned char dsm[];
     const int tid = threadIdx.x;
-    for (int i = tid; i < 65; i += kNT) sb.tab[i] = p.exptab.tab[i];
-    if (tid == 0) sb.ln2 = p.exptab.ln2;
+    load_exp_tables(p, sb);
     __syncthreads();
     // Every CTA of the cluster must have started (and initialised the shared
     // words others write into) before any remote access: arrive (release)

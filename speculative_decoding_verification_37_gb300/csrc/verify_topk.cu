@@ -517,22 +517,17 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
     extern __shared__ __align__(128) unsigned char dsm[];
     uint2 *lists = reinterpret_cast<uint2 *>(dsm);  // [2][kTopKMerge]: gathered, then unsorted kept
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const dd c2d{p.c2_hi, p.c2_lo};
-    const float2 *tab = sb.tab;
+    const DdExpTables &EK = sb.K;
     const unsigned lt = lanemask_lt();
-    for (int i = tid; i < 65; i += kNT) sb.tab[i] = p.exptab.tab[i];
+    load_exp_tables(p, sb);
     const int k = blockIdx.x / p.B, b = blockIdx.x % p.B;
     const int g = p.gamma, c = p.c;
     const int pos = b * (g + 1) + k;
     const bool has_draft = k < g;
     const int rows = has_draft ? 2 : 1;
     const unsigned K = (unsigned)p.top_k;
-    if (tid == 0) {
-        sb.ln2 = p.exptab.ln2;
-        s_bad = c > kMergeMaxC;
-    }
+    if (tid == 0) s_bad = c > kMergeMaxC;
     __syncthreads();
-    const float2 ln2 = sb.ln2;
 
     // 1. offsets and T* (warp r, row r)
     if (wid < rows && !s_bad) {
@@ -648,7 +643,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
                 if (m != -INFINITY) {
 #pragma unroll 1
                     for (int x = lane; x < kn; x += 32)
-                        S = dd_add(S, dd_expw(key_value<T>(s_kept[r][x].x), m, c2d, tab, ln2));
+                        S = dd_add(S, dd_expw(key_value<T>(s_kept[r][x].x), m, EK));
                 }
                 S = warp_dd_sum(S);
                 if (lane == 0) {
@@ -697,8 +692,8 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
         const dd isq = has_draft ? dd_recip(sq) : dd{0.0f, 0.0f};
         bool accept = false;
         if (has_draft) {
-            const dd pd = kkey<T>(l_d) >= s_th[0] ? dd_mul(dd_expw(l_d, mp, c2d, tab, ln2), isp) : dd{0.0f, 0.0f};
-            const dd qd = kkey<T>(g_d) >= s_th[1] ? dd_mul(dd_expw(g_d, mq, c2d, tab, ln2), isq) : dd{0.0f, 0.0f};
+            const dd pd = kkey<T>(l_d) >= s_th[0] ? dd_mul(dd_expw(l_d, mp, EK), isp) : dd{0.0f, 0.0f};
+            const dd qd = kkey<T>(g_d) >= s_th[1] ? dd_mul(dd_expw(g_d, mq, EK), isq) : dd{0.0f, 0.0f};
             float a;
             if (dd_pos(qd)) {
                 const dd ratio = dd_mul(pd, dd_recip(qd));
@@ -717,7 +712,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
                 const int mid = (lo + hi) >> 1;
                 if (Kq[mid].y < id) lo = mid + 1; else hi = mid;
             }
-            return (lo < nq && Kq[lo].y == id) ? dd_mul(dd_expw(key_value<T>(Kq[lo].x), mq, c2d, tab, ln2), isq)
+            return (lo < nq && Kq[lo].y == id) ? dd_mul(dd_expw(key_value<T>(Kq[lo].x), mq, EK), isq)
                                                : dd{0.0f, 0.0f};
         };
         // lane l holds kept entries [l*E, l*E + E) in token order; their p
@@ -731,7 +726,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
         dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
 #pragma unroll 1
         for (int i = i0; i < i1; ++i) {
-            const dd ex = dd_expw(key_value<T>(Kp[i].x), mp, c2d, tab, ln2);
+            const dd ex = dd_expw(key_value<T>(Kp[i].x), mp, EK);
             dd pi = ex, w = ex;
             if (has_draft) {
                 pi = dd_mul(ex, isp);
