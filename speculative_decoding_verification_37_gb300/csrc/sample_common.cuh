@@ -26,6 +26,10 @@ constexpr int kMaxCluster = 8;
 constexpr int kSeg = 256;        // candidates one top-k slice may contribute per row
 constexpr int kScanE = 8;        // elements per thread per tile of the token-order scan
 constexpr int kKeptMax = 256;    // kept (top-k) entries per row a position can sort
+constexpr int kAmbMax = 128;     // residual elements per CTA left to the exact sums (more: a full pass)
+// Margin of the residual classification: p_i > q_i is decided from the fp32
+// estimate of S_p/S_q (relative error below ~2e-5) only outside this band.
+constexpr float kAmbRel = 1.0f / 1024.0f;
 
 // Dynamic shared memory of the masked path: rows stream through a ring.
 constexpr int kRingCH = 8192, kRingNST = 4;
@@ -41,6 +45,10 @@ struct SampBase {
     float4 dsum[kMaxCluster];     // pushed dd pair of sums per rank
     float zdiag[kMaxCluster];     // pushed fp32 residual mass per rank
     unsigned cnt[2][2][kMaxCluster];
+    float4 dsum2[kMaxCluster];    // pushed residual mass (dd) per rank
+    unsigned ovfr[kMaxCluster];   // pushed list-overflow bit per rank
+    int namb;                     // ambiguous residual elements listed by this CTA
+    int amb[kAmbMax];             // their indices
     unsigned rej;                 // earliest-rejection word, pushed by rank 0
     unsigned ovf;                 // candidate-list overflow, OR-ed by every rank
     int found, lastpos, arrive_last;
@@ -531,7 +539,13 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     }
 
     if (draw) {
-        // ---- the draw in dd: slice sums (pass A), residual (pass B), scan ----
+        // ---- the draw in dd ----
+        // Pass A (L2): the CTA's slice sums S_p, S_q of both rows' terms and,
+        // over P = {i : p_i > q_i}, the sums P_p, P_q of the terms whose side
+        // the fp32 estimate of S_p/S_q decides with margin; the others are
+        // listed and resolved once the exact sums are known:
+        //   Z_w = P_p/S_p - P_q/S_q + sum over the listed i of max(0, p_i - q_i).
+        // If any CTA's list overflows, a full residual pass replaces it.
         const DdExpTables &K = sb.K;
         const float mp = Mp.m, mq = Mq.m;
         auto ep = [&](float x) -> dd {
@@ -540,14 +554,26 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
         auto eq = [&](float y) -> dd {
             return (!MASK || (fkey(y) >> KS) >= th_q) ? dd_expw(y, mq, K) : dd{0.0f, 0.0f};
         };
-        dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f};
+        if (tid == 0) sb.namb = 0;
+        __syncthreads();
+        dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f}, pp{0.0f, 0.0f}, pq{0.0f, 0.0f};
         if (has_draft) {
-            for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+            const float rho = Mp.s / Mq.s;  // fp32 estimate of S_p / S_q
+            const float rhi = rho * (1.0f + kAmbRel), rlo = rho * (1.0f - kAmbRel);
+            for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int base, int cnt) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     if (e < cnt) {
-                        sp = dd_add(sp, ep(xa[e]));
-                        sq = dd_add(sq, eq(xb[e]));
+                        const dd a = ep(xa[e]), q = eq(xb[e]);
+                        sp = dd_acc(sp, a);
+                        sq = dd_acc(sq, q);
+                        if (a.hi > q.hi * rhi) {
+                            pp = dd_acc(pp, a);
+                            pq = dd_acc(pq, q);
+                        } else if (a.hi > 0.0f && a.hi >= q.hi * rlo) {
+                            const int at = atomicAdd(&sb.namb, 1);
+                            if (at < kAmbMax) sb.amb[at] = base + e;
+                        }
                     }
                 }
             });
@@ -555,59 +581,74 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
             for_slice_vec<T, 4>(trow, lo, hi, tid, kNT, [&](const float *x, int, int cnt) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    if (e < cnt) sp = dd_add(sp, ep(x[e]));
+                    if (e < cnt) sp = dd_acc(sp, ep(x[e]));
             });
         }
         block_dd_sum2<kNT>(sp, sq, sb.redd);
-        if (tid < c) *ex.at(&sb.dsum[j], tid) = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
+        block_dd_sum2<kNT>(pp, pq, sb.redd);
+        const unsigned my_ovf = sb.namb > kAmbMax ? 1u : 0u;
+        if (tid < c) {
+            *ex.at(&sb.dsum[j], tid) = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
+            *ex.at(&sb.ovfr[j], tid) = my_ovf;
+        }
         ex.sync();
         dd Sp{0.0f, 0.0f}, Sq{0.0f, 0.0f};
-        float4 part[kMaxCluster];
+        unsigned any_ovf = 0u;
         for (int r = 0; r < c; ++r) {
             Sp = dd_add(Sp, dd{sb.dsum[r].x, sb.dsum[r].y});
             Sq = dd_add(Sq, dd{sb.dsum[r].z, sb.dsum[r].w});
-            part[r] = sb.dsum[r];
+            any_ovf |= sb.ovfr[r];
         }
         const dd isp = dd_recip(Sp);
         const dd isq = has_draft ? dd_recip(Sq) : dd{0.0f, 0.0f};
         bool use_p = true, fb = false;
-        dd total = Sp;  // bonus: weights are the unnormalised target terms
+        dd total = Sp;  // bonus and fallback: the unnormalised target terms
         if (has_draft) {
-            dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
-            for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    if (e < cnt) {
-                        const dd pi = dd_mul(ep(xa[e]), isp);
-                        const dd qi = dd_mul(eq(xb[e]), isq);
-                        zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qi))));
-                        zp = dd_add(zp, pi);
-                    }
+            // this CTA's residual mass
+            dd zw{0.0f, 0.0f};
+            if (!any_ovf) {
+                const int na = sb.namb;
+                for (int x = tid; x < na; x += kNT) {
+                    const int i = sb.amb[x];
+                    const dd pi = dd_mul(ep(ld_elem(trow, i)), isp);
+                    const dd qi = dd_mul(eq(ld_elem(drow, i)), isq);
+                    zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qi))));
                 }
-            });
-            block_dd_sum2<kNT>(zw, zp, sb.redd);
-            __syncthreads();
-            if (tid < c) *ex.at(&sb.dsum[j], tid) = make_float4(zw.hi, zw.lo, zp.hi, zp.lo);
-            ex.sync();
-            dd Zw{0.0f, 0.0f}, Zp{0.0f, 0.0f};
-            for (int r = 0; r < c; ++r) {
-                Zw = dd_add(Zw, dd{sb.dsum[r].x, sb.dsum[r].y});
-                Zp = dd_add(Zp, dd{sb.dsum[r].z, sb.dsum[r].w});
-                part[r] = sb.dsum[r];
+            } else {
+                for_slice2<T, 2>(trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        if (e < cnt) {
+                            const dd pi = dd_mul(ep(xa[e]), isp);
+                            const dd qi = dd_mul(eq(xb[e]), isq);
+                            zw = dd_add(zw, dd_max0(dd_add(pi, dd_neg(qi))));
+                        }
+                    }
+                });
             }
+            dd unused{0.0f, 0.0f};
+            block_dd_sum2<kNT>(zw, unused, sb.redd);
+            if (!any_ovf) zw = dd_add(zw, dd_add(dd_mul(pp, isp), dd_neg(dd_mul(pq, isq))));
+            __syncthreads();
+            if (tid < c) *ex.at(&sb.dsum2[j], tid) = make_float4(zw.hi, zw.lo, 0.0f, 0.0f);
+            ex.sync();
+            dd Zw{0.0f, 0.0f};
+            for (int r = 0; r < c; ++r) Zw = dd_add(Zw, dd{sb.dsum2[r].x, sb.dsum2[r].y});
             o.z = dd_to_f(Zw);
             fb = dd_le(Zw, dd{p.eps, 0.0f});
             use_p = fb;
-            total = fb ? Zp : Zw;
+            if (!fb) total = Zw;
             if (fb) o.info |= REC_FALLBACK;
         }
         const dd t = dd_mul_f(total, u_f);
         // the slice that holds the crossing (identical choice in every CTA)
         int owner = -1, lastpos = -1;
         dd acc{0.0f, 0.0f}, own_prefix{0.0f, 0.0f}, last_prefix{0.0f, 0.0f};
+        // per rank: its S_p (bonus, fallback: the unnormalised target terms) or
+        // its residual mass
+        const float4 *part = use_p ? sb.dsum : sb.dsum2;
         for (int r = 0; r < c; ++r) {
-            const dd prt = !has_draft ? dd{part[r].x, part[r].y}
-                                      : (use_p ? dd{part[r].z, part[r].w} : dd{part[r].x, part[r].y});
+            const dd prt{part[r].x, part[r].y};
             if (dd_pos(prt)) {
                 if (owner < 0 && dd_gt(dd_add(acc, prt), t)) { owner = r; own_prefix = acc; }
                 lastpos = r;
@@ -620,10 +661,8 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
         if (j == owner) {
             o.token = dd_scan_slice<kNT>(lo, hi, own_prefix, t, [&](int i) -> dd {
                 const dd e = ep(ld_elem(trow, i));
-                if (!has_draft) return e;
-                const dd pi = dd_mul(e, isp);
-                if (use_p) return pi;
-                return dd_max0(dd_add(pi, dd_neg(dd_mul(eq(ld_elem(drow, i)), isq))));
+                if (use_p) return e;
+                return dd_max0(dd_add(dd_mul(e, isp), dd_neg(dd_mul(eq(ld_elem(drow, i)), isq))));
             }, sb);
         }
     }

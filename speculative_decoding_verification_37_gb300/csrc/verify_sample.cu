@@ -36,7 +36,7 @@
 namespace specv {
 
 template <typename T, bool MASK>
-__global__ void __launch_bounds__(kNT) chain_sample_kernel(SampleParams p) {
+__global__ void __launch_bounds__(kNT, 3) chain_sample_kernel(SampleParams p) {
     __shared__ SampBase sb;
     extern __shared__ __align__(128) unsigned char dsm[];
     const int tid = threadIdx.x;
