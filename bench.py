@@ -58,15 +58,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on the current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    rec = d.get(kernel)
+    rec = d.get(f"{kernel} | {workload}")
     if not rec or rec.get("source_hash") != kernel_source_hash():
         return None
     return rec
@@ -484,10 +484,11 @@ def main():
     if wl.kind == "tree" or wl.spec.greedy:
         kname = "argmax_verify_kernel"
     elif 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
-        kname = "chain_topk_kernel"
+        # one spec_verify_chain call launches both; timed together
+        kname = "chain_topk_kernel+chain_topk_merge_kernel"
     else:
         kname = "chain_sample_kernel"
-    tr = traffic_record(kname)
+    tr = traffic_record(kname, config_dict(args.config, world, args.batch)["workload"])
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": None if tr is None else tr["bytes_per_launch"],
@@ -498,9 +499,11 @@ def main():
     if wl.kvb is not None:
         t_commit = statistics.mean(commit_ms)
         kvb = kv_bytes(wl, n_commit_total)
+        ctr = traffic_record("commit_kv_kernel", config_dict(args.config, world, args.batch)["workload"])
         commit = {"kernel": "commit_kv_kernel", "avg_launch_ms": round(t_commit, 5),
                   "algorithmic_bytes": kvb, "achieved_gbs": round(kvb / (t_commit * 1e-3) / 1e9, 1),
                   "frac": round(kvb / (t_commit * 1e-3) / 1e9 / peak, 4),
+                  "traffic": None if ctr is None else ctr["bytes_per_launch"],
                   "committed_tokens": n_commit_total}
 
     # end-to-end through the public API with host buffers
