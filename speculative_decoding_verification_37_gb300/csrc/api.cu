@@ -180,7 +180,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.rows = a->target_logits;
         p.stride = a->target_row_stride;
         p.V = a->V;
-        p.slices = slices_for(a->V, a->dtype, 1 << 20);
+        p.slices = slices_for(a->V, a->dtype, 1 << 20, argmax_stage_bytes());
         p.slice_len = slice_len(a->V, p.slices);
         p.rows_per_req = a->gamma + 1;
         p.keys = static_cast<unsigned long long *>(w.data);
@@ -194,7 +194,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.n_out = a->n_out;
         p.flags = a->flags;
         if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
-        e = launch_argmax_verify(p, a->dtype, (int)rows, s);
+        e = launch_argmax_verify(p, a->dtype, (int)rows, sm_count(), s);
     } else {
         SampleParams p = {};
         p.B = a->B;
@@ -267,7 +267,7 @@ extern "C" int spec_verify_tree(const SpecTreeArgs *a, void *workspace, size_t w
     p.rows = a->logits;
     p.stride = a->row_stride;
     p.V = a->V;
-    p.slices = slices_for(a->V, a->dtype, 1 << 20);
+    p.slices = slices_for(a->V, a->dtype, 1 << 20, argmax_stage_bytes());
     p.slice_len = slice_len(a->V, p.slices);
     p.rows_per_req = a->R;
     p.keys = static_cast<unsigned long long *>(w.data);
@@ -290,7 +290,7 @@ extern "C" int spec_verify_tree(const SpecTreeArgs *a, void *workspace, size_t w
     p.n_out = a->n_out;
     p.flags = a->flags;
     if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
-    const cudaError_t e = launch_argmax_verify(p, a->dtype, (int)rows, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_argmax_verify(p, a->dtype, (int)rows, sm_count(), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 

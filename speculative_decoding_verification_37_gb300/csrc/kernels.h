@@ -84,7 +84,8 @@ struct CommitParams {
     unsigned *flags, *status, *counters;  // counters: one per request, zero between calls
 };
 
-cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, cudaStream_t s);
+cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, int sms, cudaStream_t s);
+int argmax_stage_bytes();  // a greedy slice body must fit this
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s);
 int topk_row_bytes();  // a top-k slice body per row must fit this
