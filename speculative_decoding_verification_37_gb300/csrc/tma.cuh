@@ -17,6 +17,15 @@
 
 namespace specv {
 
+// Programmatic dependent launch: a primary kernel lets its dependent launch
+// at once; the dependent waits for the primary's completion (and its memory)
+// only where it reads the primary's results.  Both are no-ops without the
+// launch attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // bounded spin on an mbarrier phase; false if it did not complete in time
 constexpr long long kSpinLimit = 1ll << 22;
 

@@ -22,14 +22,8 @@ namespace specv {
 
 constexpr int kArgNT = 256;
 
-// Programmatic dependent launch: the pass lets the decision kernel launch at
-// once; the decision kernel waits for the pass's completion (and its memory)
-// only where it reads the argmax keys.  Both are no-ops without the launch
-// attribute.
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// (The decision kernel is a programmatic dependent launch of the pass, see
+// tma.cuh: it waits for the pass only where it reads the argmax keys.)
 constexpr int kMaxMaskWords = 32;  // trees of up to 1023 draft nodes
 
 // -- chain decision (warp 0; lane k takes position k) ---------------------------

@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
     TkRing &R = *reinterpret_cast<TkRing *>(dsm);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const unsigned lt = lanemask_lt();
+    pdl_launch_dependents();  // the merge may launch and run its prologue
 
     // gridDim.x is a multiple of c: every item of this block is slice j
     const int c = p.c, B = p.B;
@@ -528,6 +529,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
     const unsigned K = (unsigned)p.top_k;
     if (tid == 0) s_bad = c > kMergeMaxC;
     __syncthreads();
+    pdl_wait_primary();  // the HBM pass's regions and records are complete
 
     // 1. offsets and T* (warp r, row r)
     if (wid < rows && !s_bad) {
@@ -782,6 +784,22 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
 static_assert(2 * kTopKMerge * sizeof(uint2) <= kSampDyn, "the merged lists fit the fallback ring's memory");
 static_assert(kKeptMax % 32 == 0, "kept entries split evenly over a warp's lanes");
 
+// launches `k` as a programmatic dependent of the previous kernel in `s`
+template <typename K>
+static cudaError_t launch_pdl(K k, dim3 grid, int smem, cudaStream_t s, const SampleParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kNT);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s) {
     // a multiple of c (each block keeps one slice index), at most a full wave
     const int64_t items = (int64_t)p.B * (p.gamma + 1) * p.c;
@@ -799,14 +817,16 @@ cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStr
         if (e == cudaSuccess) e = ensure_smem_attr(chain_topk_merge_kernel<__nv_bfloat16>, msmem, mdone);
         if (e != cudaSuccess) return e;
         chain_topk_kernel<__nv_bfloat16><<<grid, kNT, smem, s>>>(p);
-        chain_topk_merge_kernel<__nv_bfloat16><<<mgrid, kNT, msmem, s>>>(p);
+        e = launch_pdl(chain_topk_merge_kernel<__nv_bfloat16>, mgrid, msmem, s, p);
+        if (e != cudaSuccess) return e;
     } else {
         static std::atomic<unsigned long long> done{0}, mdone{0};
         e = ensure_smem_attr(chain_topk_kernel<float>, smem, done);
         if (e == cudaSuccess) e = ensure_smem_attr(chain_topk_merge_kernel<float>, msmem, mdone);
         if (e != cudaSuccess) return e;
         chain_topk_kernel<float><<<grid, kNT, smem, s>>>(p);
-        chain_topk_merge_kernel<float><<<mgrid, kNT, msmem, s>>>(p);
+        e = launch_pdl(chain_topk_merge_kernel<float>, mgrid, msmem, s, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
