@@ -19,8 +19,8 @@
 //     logit >= it).  The block reuses the bound of its previous item (the
 //     same slice of another position, with similar logits) when the vectors
 //     reaching it prove it valid for this one, and otherwise searches a new
-//     one: the ceil(1.5 K)-th largest of the threads' maxima (warp r, row r,
-//     a bitwise search with warp reductions).
+//     one: the K-th largest of the threads' maxima (warp r, row r, a bitwise
+//     search with warp reductions).
 //  3. Few vectors can hold a logit >= the bound; each warp lists those whose
 //     maximum reaches it, and groups of lanes test the listed vectors element
 //     by element.  The candidates, (order key, token id), gather in shared
@@ -42,7 +42,7 @@ namespace specv {
 constexpr int kTkNST = 2;             // ring stages (items in flight per block)
 constexpr int kTkRowBytes = 16384;    // one row's slice body per stage
 constexpr int kTkBlocksPerSM = 3;
-constexpr int kTkFastRounds = 4;      // listed vectors per warp tested in registers: 4 * 32 / VEC
+constexpr int kTkRounds = 4;          // rounds of 8 listed vectors a warp tests into registers at once
 
 constexpr int kTkVecPerThr = kTkRowBytes / 16 / kNT;  // 16-byte vectors per thread and row
 static_assert(kTkVecPerThr * 16 * kNT == kTkRowBytes, "a stage row is whole vectors per thread");
@@ -175,6 +175,22 @@ template <> __device__ __forceinline__ float vec_elem<__nv_bfloat16>(const uint4
     return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
 }
 
+// bit e set iff element e of a 32-bit word (2 bf16 or 1 f32) is >= t
+template <typename T> __device__ __forceinline__ uint32_t word_ge_mask(uint32_t w, float t);
+template <> __device__ __forceinline__ uint32_t word_ge_mask<float>(uint32_t w, float t) {
+    return __uint_as_float(w) >= t ? 1u : 0u;
+}
+template <> __device__ __forceinline__ uint32_t word_ge_mask<__nv_bfloat16>(uint32_t w, float t) {
+    const uint32_t m = __hge2_mask(as_bf2(w), __float2bfloat162_rn(t));  // exact: t is a bf16 value or -inf
+    return (m & 1u) | ((m >> 15) & 2u);
+}
+// element e of a 32-bit word
+template <typename T> __device__ __forceinline__ float word_elem(uint32_t w, int e);
+template <> __device__ __forceinline__ float word_elem<float>(uint32_t w, int) { return __uint_as_float(w); }
+template <> __device__ __forceinline__ float word_elem<__nv_bfloat16>(uint32_t w, int e) {
+    return __uint_as_float(e ? (w & 0xffff0000u) : (w << 16));
+}
+
 // The K-th largest of kNT keys (one per thread of the block, in smem) by
 // one warp: the largest r with at least K keys >= r, fixed two bits per step
 // (three independent counts) and only over the bits in which the smallest
@@ -216,7 +232,6 @@ __device__ __forceinline__ uint32_t warp_kth_of_block(const uint32_t *keys, unsi
 template <typename T>
 __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleParams p) {
     constexpr int VEC = Elem<T>::VEC;
-    constexpr int GROUPS = 32 / VEC;  // hit vectors a warp examines per round
     __shared__ __align__(8) unsigned long long full[kTkNST];
     // the thread maxima are dead before the first candidate is written, and
     // the candidates of the previous item are out before the maxima are
@@ -243,9 +258,9 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
     const int sk = qstep / B, sb = qstep - sk * B;
     const int npos = B * (p.gamma + 1);
     const unsigned K = (unsigned)p.top_k;
-    // the bound is searched as the Kq-th largest thread maximum (Kq >= K, a
-    // little below the K-th, so that it stays valid for the next rows)
-    const unsigned Kq = min((unsigned)kNT, K + (K + 1) / 2);
+    // the bound is searched as the K-th largest thread maximum; reused for the
+    // next rows while at least K of their vector maxima reach it
+    const unsigned Kq = min((unsigned)kNT, K);
     unsigned phase = 0u;  // bit s: parity of stage s's next completion
     bool timeout = false;
     uint32_t guess[2] = {0xffffffffu, 0xffffffffu};  // reused bound per row (key); none yet
@@ -363,51 +378,53 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
                     base = __shfl_sync(kFull, base, 0) + __popc(bal & lt);
                     if (pred && base < (unsigned)kTopKSlicePool) s_cand[r][base] = make_uint2(kkey<T>(x), (uint32_t)idx);
                 };
-                if (nh[r] <= kTkFastRounds * GROUPS) {
-                    // few listed vectors (the usual case): test them all, then
-                    // one shared-memory atomic for the warp
-                    bool pred[kTkFastRounds];
-                    uint32_t key[kTkFastRounds], idx[kTkFastRounds], bal[kTkFastRounds];
-                    unsigned wtot = 0u;
+                // each lane takes one 32-bit word of a listed vector (4 words a
+                // vector, 8 vectors a round); up to kTkRounds rounds are tested
+                // into registers, then one shared-memory atomic places the warp's
+                // candidates
+                const uint32_t *stw = reinterpret_cast<const uint32_t *>(stage);
+                const int nrounds = (nh[r] + 7) / 8;
+                for (int r0 = 0; r0 < nrounds; r0 += kTkRounds) {
+                    uint32_t mk[kTkRounds], wd[kTkRounds];
+                    int qv[kTkRounds];
+                    unsigned mine = 0u;
 #pragma unroll
-                    for (int rr = 0; rr < kTkFastRounds; ++rr) {
-                        const int h = rr * GROUPS + lane / VEC, e = lane % VEC;
-                        pred[rr] = false;
-                        key[rr] = idx[rr] = 0u;
-                        if (h < nh[r]) {
-                            const int q = s_hits[r][wid][h];
-                            const float x = to_f32(stage[q * VEC + e]);
-                            pred[rr] = x >= tf[r];
-                            key[rr] = kkey<T>(x);
-                            idx[rr] = (uint32_t)(sp.body0 + q * VEC + e);
-                        }
-                        bal[rr] = __ballot_sync(kFull, pred[rr]);
-                        wtot += __popc(bal[rr]);
-                    }
-                    if (wtot) {
-                        unsigned base = 0u;
-                        if (lane == 0) base = atomicAdd(&s_ccnt[r], wtot);
-                        base = __shfl_sync(kFull, base, 0);
-#pragma unroll
-                        for (int rr = 0; rr < kTkFastRounds; ++rr) {
-                            const unsigned at = base + __popc(bal[rr] & lt);
-                            if (pred[rr] && at < (unsigned)kTopKSlicePool) s_cand[r][at] = make_uint2(key[rr], idx[rr]);
-                            base += __popc(bal[rr]);
+                    for (int rr = 0; rr < kTkRounds; ++rr) {
+                        mk[rr] = 0u;
+                        wd[rr] = 0u;
+                        qv[rr] = 0;
+                        if (r0 + rr < nrounds) {  // warp-uniform
+                            const int h = (r0 + rr) * 8 + (lane >> 2);
+                            if (h < nh[r]) {
+                                qv[rr] = s_hits[r][wid][h];
+                                wd[rr] = stw[qv[rr] * 4 + (lane & 3)];
+                                mk[rr] = word_ge_mask<T>(wd[rr], tf[r]);
+                                mine += __popc(mk[rr]);
+                            }
                         }
                     }
-                } else {
-                    for (int h0 = 0; h0 < nh[r]; h0 += GROUPS) {
-                        const int h = h0 + lane / VEC, e = lane % VEC;
-                        bool pred = false;
-                        float x = 0.0f;
-                        int idx = 0;
-                        if (h < nh[r]) {
-                            const int q = s_hits[r][wid][h];
-                            x = to_f32(stage[q * VEC + e]);
-                            pred = x >= tf[r];
-                            idx = sp.body0 + q * VEC + e;
+                    unsigned incl = mine;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned y = __shfl_up_sync(kFull, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const unsigned wtot = __shfl_sync(kFull, incl, 31);
+                    if (wtot == 0u) continue;
+                    unsigned base = 0u;
+                    if (lane == 31) base = atomicAdd(&s_ccnt[r], wtot);
+                    unsigned at = __shfl_sync(kFull, base, 31) + incl - mine;
+#pragma unroll
+                    for (int rr = 0; rr < kTkRounds; ++rr) {
+                        uint32_t m = mk[rr];
+                        while (m) {
+                            const int e = __ffs(m) - 1;
+                            m &= m - 1u;
+                            if (at < (unsigned)kTopKSlicePool)
+                                s_cand[r][at] = make_uint2(kkey<T>(word_elem<T>(wd[rr], e)),
+                                                           (uint32_t)(sp.body0 + qv[rr] * VEC + (lane & 3) * (VEC / 4) + e));
+                            ++at;
                         }
-                        emit(pred, x, idx);
                     }
                 }
                 if (wid == 0 && (nhead | ntail)) {
