@@ -42,7 +42,8 @@ namespace specv {
 constexpr int kTkNST = 2;             // ring stages (items in flight per block)
 constexpr int kTkRowBytes = 16384;    // one row's slice body per stage
 constexpr int kTkBlocksPerSM = 3;
-constexpr int kTkRounds = 4;          // rounds of 8 listed vectors a warp tests into registers at once
+// a region entry for a scalar head or tail logit rather than a 16-byte vector
+constexpr uint32_t kScalarEntry = 0x80000000u;
 
 constexpr int kTkVecPerThr = kTkRowBytes / 16 / kNT;  // 16-byte vectors per thread and row
 static_assert(kTkVecPerThr * 16 * kNT == kTkRowBytes, "a stage row is whole vectors per thread");
@@ -232,19 +233,11 @@ __device__ __forceinline__ uint32_t warp_kth_of_block(const uint32_t *keys, unsi
 template <typename T>
 __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleParams p) {
     constexpr int VEC = Elem<T>::VEC;
+    constexpr int SLOTS = kTkVecPerThr + 2;  // a thread's vectors, then its head and tail scalar
     __shared__ __align__(8) unsigned long long full[kTkNST];
-    // the thread maxima are dead before the first candidate is written, and
-    // the candidates of the previous item are out before the maxima are
-    __shared__ union {
-        uint32_t max[2][kNT];
-        uint2 cand[2][kTopKSlicePool];
-    } s_u;
-    auto &s_max = s_u.max;
-    auto &s_cand = s_u.cand;
+    __shared__ uint32_t s_max[2][kNT];
     __shared__ uint32_t s_t0[2];
-    __shared__ unsigned s_hcnt[2][kNW];
-    __shared__ unsigned s_ccnt[2];
-    __shared__ uint16_t s_hits[2][kNW][32 * kTkVecPerThr];
+    __shared__ unsigned s_hcnt[2][2][kNW];  // [item parity][row][warp]
     extern __shared__ __align__(128) unsigned char dsm[];
     TkRing &R = *reinterpret_cast<TkRing *>(dsm);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -258,9 +251,6 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
     const int sk = qstep / B, sb = qstep - sk * B;
     const int npos = B * (p.gamma + 1);
     const unsigned K = (unsigned)p.top_k;
-    // the bound is searched as the K-th largest thread maximum; reused for the
-    // next rows while at least K of their vector maxima reach it
-    const unsigned Kq = min((unsigned)kNT, K);
     unsigned phase = 0u;  // bit s: parity of stage s's next completion
     bool timeout = false;
     uint32_t guess[2] = {0xffffffffu, 0xffffffffu};  // reused bound per row (key); none yet
@@ -279,7 +269,7 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
     __syncthreads();
 
     for (int t = 0; cur.qpos < npos; cur.step(qstep, sk, sb, B), ++t) {
-        const int s = t % kTkNST;
+        const int s = t % kTkNST, par = t & 1;
         const TkItem<T> it = tk_item<T>(p, cur.k, cur.b, j);
         const SliceSplit sp = it.sp;
         const int nhead = sp.body0 - sp.head0, ntail = sp.hi - sp.tail0;
@@ -297,23 +287,8 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
         phase ^= 1u << s;
         const int nvec = it.ok ? (sp.tail0 - sp.body0) / VEC : 0;
 
-        // 1. largest logit per 16-byte vector and per thread; the vectors that
-        //    reach the reused bound, listed per warp
+        // 1. largest logit per 16-byte vector and per thread
         float vm[2][kTkVecPerThr], mt[2];
-        int nh[2] = {0, 0};
-        float tf[2];
-        auto list_hits = [&](int r) {
-            int n = 0;
-#pragma unroll
-            for (int i = 0; i < kTkVecPerThr; ++i) {
-                const bool hit = tid + i * kNT < nvec && vm[r][i] >= tf[r];
-                const unsigned bal = __ballot_sync(kFull, hit);
-                if (hit) s_hits[r][wid][n + __popc(bal & lt)] = (uint16_t)(tid + i * kNT);
-                n += __popc(bal);
-            }
-            nh[r] = n;
-            if (lane == 0) s_hcnt[r][wid] = (unsigned)n;
-        };
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const uint4 *src = reinterpret_cast<const uint4 *>(R.buf[s][r]);
@@ -325,14 +300,45 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
                 m = fmaxf(m, vm[r][i]);
             }
             mt[r] = m;
+        }
+        // 2. the vectors (and scalars) that reach the row's bound: a bit per
+        //    slot and the slot's rank among the warp's hits
+        float tf[2];
+        uint32_t hits[2] = {0u, 0u}, ranks[2][2] = {{0u, 0u}, {0u, 0u}};  // 8-bit ranks, 4 slots per word
+        auto list_hits = [&](int r) {
+            unsigned n = 0;
+            uint32_t h = 0u, rk0 = 0u, rk1 = 0u;
+#pragma unroll
+            for (int i = 0; i < SLOTS; ++i) {
+                bool hit;
+                if (i < kTkVecPerThr) hit = tid + i * kNT < nvec && vm[r][i] >= tf[r];
+                else if (i == kTkVecPerThr) hit = tid < nhead && xh[r] >= tf[r];
+                else hit = tid < ntail && xt[r] >= tf[r];
+                const unsigned bal = __ballot_sync(kFull, hit);
+                const uint32_t rk = n + __popc(bal & lt);
+                if (i < 4) rk0 |= rk << (8 * i); else rk1 |= rk << (8 * (i - 4));
+                h |= (hit ? 1u : 0u) << i;
+                n += __popc(bal);
+            }
+            hits[r] = h;
+            ranks[r][0] = rk0;
+            ranks[r][1] = rk1;
+            if (lane == 0) s_hcnt[par][r][wid] = n;
+        };
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
             tf[r] = keep_all ? -INFINITY : (guess[r] == 0xffffffffu ? INFINITY : key_value<T>(guess[r]));
             if (r < it.rows && it.ok) list_hits(r);
         }
-        __syncthreads();  // hit counts; the previous item's candidates are out
+        __syncthreads();  // hit counts; stage s is consumed (the maxima are in registers)
+        if (tid == 0) {
+            if (nxt.qpos < npos) tk_issue<T>(p, R, full, nxt, j, s);  // refill stage s
+            nxt.step(qstep, sk, sb, B);
+        }
 
-        // 2. the reused bound holds for this slice if at least K listed vectors
+        // 3. the reused bound holds for this slice if at least K listed slots
         //    reach it (each holds a logit >= it); otherwise (or if it lets in
-        //    too many) search the Kq-th largest thread maximum again
+        //    too many) search the K-th largest thread maximum again
         bool redo[2] = {false, false};
         if (it.ok && !keep_all) {
 #pragma unroll
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
                 if (r >= it.rows) break;
                 unsigned tot = 0;
 #pragma unroll
-                for (int w = 0; w < kNW; ++w) tot += s_hcnt[r][w];
+                for (int w = 0; w < kNW; ++w) tot += s_hcnt[par][r][w];
                 redo[r] = tot < K || tot > (unsigned)(kTopKSlicePool / 2);
             }
         }
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
             for (int r = 0; r < it.rows; ++r) s_max[r][tid] = kkey<T>(mt[r]);
             __syncthreads();
             if (wid < it.rows && (wid == 0 ? redo[0] : redo[1])) {
-                const uint32_t t0 = warp_kth_of_block(s_max[wid], Kq);
+                const uint32_t t0 = warp_kth_of_block(s_max[wid], min(K, (unsigned)kNT));
                 if (lane == 0) s_t0[wid] = t0;
             }
             __syncthreads();
@@ -359,96 +365,39 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
                 tf[r] = key_value<T>(guess[r]);
                 list_hits(r);
             }
+            __syncthreads();
         }
-        if (tid < it.rows) s_ccnt[tid] = 0u;
-        __syncthreads();
 
-        // 3. candidates: groups of VEC lanes test one listed vector element by
-        //    element; found logits go to the row's list in shared memory
+        // 4. the listed slots go out to the item's regions as (order key of the
+        //    vector maximum or scalar, element index; scalars flagged); thread 0
+        //    stores the count and the bound
         if (it.ok) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 if (r >= it.rows) break;
-                const T *stage = reinterpret_cast<const T *>(R.buf[s][r]);
-                auto emit = [&](bool pred, float x, int idx) {
-                    const unsigned bal = __ballot_sync(kFull, pred);
-                    if (bal == 0u) return;
-                    unsigned base = 0u;
-                    if (lane == 0) base = atomicAdd(&s_ccnt[r], (unsigned)__popc(bal));
-                    base = __shfl_sync(kFull, base, 0) + __popc(bal & lt);
-                    if (pred && base < (unsigned)kTopKSlicePool) s_cand[r][base] = make_uint2(kkey<T>(x), (uint32_t)idx);
-                };
-                // each lane takes one 32-bit word of a listed vector (4 words a
-                // vector, 8 vectors a round); up to kTkRounds rounds are tested
-                // into registers, then one shared-memory atomic places the warp's
-                // candidates
-                const uint32_t *stw = reinterpret_cast<const uint32_t *>(stage);
-                const int nrounds = (nh[r] + 7) / 8;
-                for (int r0 = 0; r0 < nrounds; r0 += kTkRounds) {
-                    uint32_t mk[kTkRounds], wd[kTkRounds];
-                    int qv[kTkRounds];
-                    unsigned mine = 0u;
+                unsigned base = 0u, total = 0u;
 #pragma unroll
-                    for (int rr = 0; rr < kTkRounds; ++rr) {
-                        mk[rr] = 0u;
-                        wd[rr] = 0u;
-                        qv[rr] = 0;
-                        if (r0 + rr < nrounds) {  // warp-uniform
-                            const int h = (r0 + rr) * 8 + (lane >> 2);
-                            if (h < nh[r]) {
-                                qv[rr] = s_hits[r][wid][h];
-                                wd[rr] = stw[qv[rr] * 4 + (lane & 3)];
-                                mk[rr] = word_ge_mask<T>(wd[rr], tf[r]);
-                                mine += __popc(mk[rr]);
-                            }
-                        }
-                    }
-                    unsigned incl = mine;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned y = __shfl_up_sync(kFull, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    const unsigned wtot = __shfl_sync(kFull, incl, 31);
-                    if (wtot == 0u) continue;
-                    unsigned base = 0u;
-                    if (lane == 31) base = atomicAdd(&s_ccnt[r], wtot);
-                    unsigned at = __shfl_sync(kFull, base, 31) + incl - mine;
-#pragma unroll
-                    for (int rr = 0; rr < kTkRounds; ++rr) {
-                        uint32_t m = mk[rr];
-                        while (m) {
-                            const int e = __ffs(m) - 1;
-                            m &= m - 1u;
-                            if (at < (unsigned)kTopKSlicePool)
-                                s_cand[r][at] = make_uint2(kkey<T>(word_elem<T>(wd[rr], e)),
-                                                           (uint32_t)(sp.body0 + qv[rr] * VEC + (lane & 3) * (VEC / 4) + e));
-                            ++at;
-                        }
-                    }
+                for (int w = 0; w < kNW; ++w) {
+                    const unsigned cw = s_hcnt[par][r][w];
+                    base += w < wid ? cw : 0u;
+                    total += cw;
                 }
-                if (wid == 0 && (nhead | ntail)) {
-                    emit(tid < nhead && xh[r] >= tf[r], xh[r], sp.head0 + tid);
-                    emit(tid < ntail && xt[r] >= tf[r], xt[r], sp.tail0 + tid);
-                }
-            }
-        }
-        __syncthreads();  // lists complete; stage s is no longer read
-        if (tid == 0) {
-            if (nxt.qpos < npos) tk_issue<T>(p, R, full, nxt, j, s);  // refill stage s
-            nxt.step(qstep, sk, sb, B);
-        }
-
-        // 4. the lists into the item's regions; thread 0 stores the counts
-        if (it.ok) {
-            for (int r = 0; r < it.rows; ++r) {
-                const unsigned n = s_ccnt[r];
                 const int64_t reg = tk_region(p, it.pos, r, j);
+                // total > kTopKSlicePool: overflow, the merge takes the exact path
+                if (tid == 0) p.slicecb[reg] = make_uint2(total, keep_all ? 0u : kkey<T>(tf[r]));
                 uint2 *dst = p.pool + reg * kTopKSlicePool;
-                const unsigned m = min(n, (unsigned)kTopKSlicePool);
-                for (unsigned x = tid; x < m; x += kNT) dst[x] = s_cand[r][x];
-                // n > kTopKSlicePool: overflow, the merge takes the exact path
-                if (tid == 0) p.slicecb[reg] = make_uint2(n, keep_all ? 0u : kkey<T>(tf[r]));
+                const uint32_t h = hits[r];
+#pragma unroll
+                for (int i = 0; i < SLOTS; ++i) {
+                    if (!(h & (1u << i))) continue;
+                    const uint32_t at = base + ((ranks[r][i >> 2] >> (8 * (i & 3))) & 0xffu);
+                    if (at >= (uint32_t)kTopKSlicePool) continue;
+                    uint2 e;
+                    if (i < kTkVecPerThr) e = make_uint2(kkey<T>(vm[r][i]), (uint32_t)(sp.body0 + (tid + i * kNT) * VEC));
+                    else if (i == kTkVecPerThr) e = make_uint2(kkey<T>(xh[r]), (uint32_t)(sp.head0 + tid) | kScalarEntry);
+                    else e = make_uint2(kkey<T>(xt[r]), (uint32_t)(sp.tail0 + tid) | kScalarEntry);
+                    dst[at] = e;
+                }
             }
         } else if (tid < it.rows) {
             // poison: the merge takes the exact path
@@ -479,9 +428,47 @@ __global__ void __launch_bounds__(kNT, kTkBlocksPerSM) chain_topk_kernel(SampleP
 // ---------------------------------------------------------------------------
 constexpr int kMergeMaxC = 256;  // slices per row the merge can take
 
-// the K-th largest key of n entries (smem), by one warp; every lane gets it
+// the K-th largest key of n entries (smem), by one warp; every lane gets it.
+// Up to 256 keys are held in registers (8 per lane); counts are ballots.
 __device__ __forceinline__ uint32_t warp_kth_entries(const uint2 *L, int n, unsigned K) {
+    constexpr int PER = 8;
     const int lane = threadIdx.x & 31;
+    if (n <= 32 * PER) {
+        uint32_t v[PER];
+        uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int x = lane + 32 * e;
+            v[e] = x < n ? L[x].x : 0u;
+            if (x < n) {
+                lo = min(lo, v[e]);
+                hi = max(hi, v[e]);
+            }
+        }
+        lo = __reduce_min_sync(kFull, lo);
+        hi = __reduce_max_sync(kFull, hi);
+        if (lo >= hi) return lo;
+        const int rows = (n + 31) / 32;  // warp-uniform
+        auto count_ge = [&](uint32_t cand) {
+            unsigned c = 0;
+#pragma unroll
+            for (int e = 0; e < PER; ++e)
+                if (e < rows) c += __popc(__ballot_sync(kFull, lane + 32 * e < n && v[e] >= cand));
+            return c;
+        };
+        int nb = 32 - __clz(lo ^ hi);
+        uint32_t res = nb == 32 ? 0u : (hi >> nb) << nb;
+#pragma unroll 1
+        while (nb >= 2) {
+            nb -= 2;
+            const unsigned c1 = count_ge(res | (1u << nb));
+            const unsigned c2 = count_ge(res | (2u << nb));
+            const unsigned c3 = count_ge(res | (3u << nb));
+            res |= (c3 >= K ? 3u : c2 >= K ? 2u : c1 >= K ? 1u : 0u) << nb;
+        }
+        if (nb == 1 && count_ge(res | 1u) >= K) res |= 1u;
+        return res;
+    }
     uint32_t lo = 0xffffffffu, hi = 0u;
     for (int x = lane; x < n; x += 32) {
         lo = min(lo, L[x].x);
@@ -494,8 +481,8 @@ __device__ __forceinline__ uint32_t warp_kth_entries(const uint2 *L, int n, unsi
     uint32_t res = nb == 32 ? 0u : (hi >> nb) << nb;
     auto count_ge = [&](uint32_t cand) {
         unsigned c = 0;
-        for (int x = lane; x < n; x += 32) c += L[x].x >= cand;
-        return __reduce_add_sync(kFull, c);
+        for (int x0 = 0; x0 < n; x0 += 32) c += __popc(__ballot_sync(kFull, x0 + lane < n && L[x0 + lane].x >= cand));
+        return c;
     };
 #pragma unroll 1
     while (nb >= 2) {
@@ -544,6 +531,8 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
     const bool has_draft = k < g;
     const int rows = has_draft ? 2 : 1;
     const unsigned K = (unsigned)p.top_k;
+    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride;
+    const T *drow = has_draft ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
     if (tid == 0) s_bad = c > kMergeMaxC;
     __syncthreads();
     pdl_wait_primary();  // the HBM pass's regions and records are complete
@@ -627,24 +616,70 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
         }
         __syncthreads();
 
-        // 3. warp r: exact threshold, kept set in token order, row statistics
+        // 3. warp r: B, the K-th largest listed key (at least K logits of the
+        //    row reach it: every listed vector holds its maximum), the listed
+        //    vectors reaching B fetched from the row and split into their
+        //    logits >= B, the exact threshold among those, the kept set in
+        //    token order, row statistics
         if (wid < rows) {
             const int r = wid;
-            const uint2 *L = lists + r * kTopKMerge;
+            const T *row = r == 0 ? trow : drow;
+            uint2 *L = lists + r * kTopKMerge;
             const int n = s_n[r];
-            const uint32_t th = warp_kth_entries(L, n, min(K, (unsigned)n));
-            // the kept entries, compacted after the gathered ones
-            uint2 *tmp = lists + r * kTopKMerge + n;
-            int kn = 0;
+            const uint32_t bk = warp_kth_entries(L, n, min(K, (unsigned)n));
+            // candidates (order key, token id) after the gathered entries
+            uint2 *cand = L + n;
+            const int cap = kTopKMerge - n;
+            int nc = 0;
             for (int x0 = 0; x0 < n; x0 += 32) {
                 const int x = x0 + lane;
-                const bool keep = x < n && L[x].x >= th;
+                uint32_t mk = 0u;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                uint2 e = make_uint2(0u, 0u);
+                if (x < n && L[x].x >= bk) {
+                    e = L[x];
+                    if (e.y & kScalarEntry) {
+                        mk = 1u;
+                    } else {
+                        v = ld_nc16(reinterpret_cast<const uint4 *>(row + e.y));
+                        mk = vec_ge_mask<T>(v, key_value<T>(bk));
+                    }
+                }
+                const unsigned cnt = __popc(mk);
+                unsigned incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int at = nc + (int)(incl - cnt);
+                while (mk) {
+                    const int q = __ffs(mk) - 1;
+                    mk &= mk - 1u;
+                    if (at < cap) {
+                        cand[at] = (e.y & kScalarEntry) ? make_uint2(e.x, e.y & ~kScalarEntry)
+                                                        : make_uint2(kkey<T>(vec_elem<T>(v, q)), e.y + (uint32_t)q);
+                    }
+                    ++at;
+                }
+                nc += (int)__shfl_sync(kFull, incl, 31);
+            }
+            __syncwarp();
+            const int ncu = min(nc, cap);
+            // the kept logits: the candidates among the row's K largest
+            int kn = 0;
+            uint2 *tmp = cand + ncu;
+            const int cap2 = cap - ncu;
+            const uint32_t th = warp_kth_entries(cand, ncu, min(K, (unsigned)ncu));
+            for (int x0 = 0; x0 < ncu; x0 += 32) {
+                const int x = x0 + lane;
+                const bool keep = x < ncu && cand[x].x >= th;
                 const unsigned bal = __ballot_sync(kFull, keep);
                 const int at = kn + __popc(bal & lt);
-                if (keep && at < kKeptMax && n + at < kTopKMerge) tmp[at] = L[x];
+                if (keep && at < kKeptMax && at < cap2) tmp[at] = cand[x];
                 kn += __popc(bal);
             }
-            const bool fits = kn <= kKeptMax && n + kn <= kTopKMerge;
+            const bool fits = nc <= cap && kn <= kKeptMax && kn <= cap2;
             if (fits) {
                 __syncwarp();
                 for (int x = lane; x < kn; x += 32) {
@@ -688,8 +723,6 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
     if (wid != 0) return;
 
     // 4. warp 0: acceptance, residual mass, the draw
-    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride;
-    const T *drow = has_draft ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
     const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
     const bool bad_tok = has_draft && (d < 0 || d >= p.V);
     const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
