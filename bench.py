@@ -41,11 +41,37 @@ L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_37_gb300", "csrc")
 
 
+def _code_only(src: str) -> str:
+    """C/CUDA source with comments removed and whitespace collapsed, so that a
+    comment edit does not invalidate a profile taken on the same code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        ch = src[i]
+        if ch == '"' or ch == "'":  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and src[j] != ch:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(CSRC, f), "r", encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -483,7 +509,7 @@ def main():
     t_verify = statistics.mean(verify_ms)
     achieved = wl.logit_bytes / (t_verify * 1e-3) / 1e9
     if wl.kind == "tree" or wl.spec.greedy:
-        kname = "argmax_verify_kernel"
+        kname = "argmax_pass_kernel+argmax_decide_kernel"
     elif 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
         # one spec_verify_chain call launches both; timed together
         kname = "chain_topk_kernel+chain_topk_merge_kernel"

@@ -21,20 +21,26 @@
 //     reaching it prove it valid for this one, and otherwise searches a new
 //     one: the K-th largest of the threads' maxima (warp r, row r, a bitwise
 //     search with warp reductions).
-//  3. Few vectors can hold a logit >= the bound; each warp lists those whose
-//     maximum reaches it, and groups of lanes test the listed vectors element
-//     by element.  The candidates, (order key, token id), gather in shared
-//     memory and go out to the item's own region of the workspace with their
-//     count.  No global atomics, no fences, three block barriers per item
-//     (five when the bound is searched again).
+//  3. Each warp lists the 16-byte vectors (and head/tail scalars) whose
+//     maximum reaches the bound, ranked by ballots.  The entries, (order key
+//     of the vector's maximum, element index of its first logit; scalars
+//     flagged), go out to the item's own region of the workspace with the
+//     count and the bound.  No element of a vector is looked at here, no
+//     global atomics, no fences, two block barriers per item (four when the
+//     bound is searched again).
 //
-// chain_topk_merge_kernel: one block per position gathers its slices'
-// regions into shared memory and merges them exactly (compact_position:
-// block select, kept set in token order, double-float acceptance, residual
-// and draw).  A slice that overflowed its region, rows whose 16-byte phases
-// differ, or a kept set too large for the merge (hundreds of tied logits)
-// send the position to the exact masked computation over the whole row in
-// that block instead (slow, exact, rare).
+// chain_topk_merge_kernel, a programmatic dependent launch of the pass (its
+// prologue overlaps the pass's tail): one block per position gathers the
+// listed entries >= T*, the largest slice bound, into shared memory; per row,
+// the K-th largest listed key B is a lower bound of the row's K-th largest
+// logit, so only the listed vectors whose maximum reaches B are loaded again
+// (a few hundred bytes, from L2 or HBM), split into their logits >= B, and
+// the exact K-th largest among those is the threshold.  The kept set in
+// token order, the double-float acceptance, residual and draw follow.  A
+// slice that overflowed its region, rows whose 16-byte phases differ, or a
+// kept set too large for the merge (hundreds of tied logits) send the
+// position to the exact masked computation over the whole row in that block
+// instead (slow, exact, rare).
 #include "sample_common.cuh"
 
 namespace specv {
