@@ -230,6 +230,7 @@ class Step:
 
     def __init__(self, wl: Workload):
         from speculative_decoding_verification_37_gb300 import _lib as L
+        from speculative_decoding_verification_37_gb300 import api
         self.wl = wl
         s, dev, inp = wl.spec, wl.device, wl.inputs
         i32 = dict(dtype=torch.int32, device=dev)
@@ -253,7 +254,7 @@ class Step:
             g = s.gamma
             self.out = dict(n_acc=torch.empty(B, **i32), out_tokens=torch.empty((B, g + 1), **i32),
                             n_out=torch.empty(B, **i32), flags=torch.empty(B, **i32))
-            kind = L.SPEC_WS_CHAIN_TOPK if (not s.greedy and 0 < s.top_k <= L.TOPK_FAST_MAX) else L.SPEC_WS_CHAIN
+            kind = api.chain_workspace_kind(not s.greedy, s.top_k, s.V)
             self.ws = L.new_workspace(kind, B, g, s.V, dev)
 
             def verify():
@@ -513,6 +514,9 @@ def main():
     elif 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
         # one spec_verify_chain call launches both; timed together
         kname = "chain_topk_kernel+chain_topk_merge_kernel"
+    elif (wl.spec.top_k == 0 or wl.spec.top_k >= wl.spec.V) and \
+            wl.rows * -(-wl.spec.V * wl.spec.esize // 4096) >= 1024:
+        kname = "chain_full_kernel"  # the persistent full-vocabulary path (at least 1,024 4 KiB items)
     else:
         kname = "chain_sample_kernel"
     tr = traffic_record(kname, config_dict(args.config, world, args.batch)["workload"])

@@ -68,8 +68,9 @@ extern "C" {
 #define SPEC_FLAG_BAD_INPUT 1u  /* token / node / slot / block id out of range: request skipped */
 #define SPEC_FLAG_FALLBACK 2u   /* residual mass <= fallback_eps: the draw used p_k itself */
 #define SPEC_FLAG_BAD_ROW 4u    /* every kept logit of a row is -inf: request skipped */
-#define SPEC_FLAG_TIMEOUT 8u    /* a bulk copy did not complete within its wait limit (status word
-                                   only): outputs of the call are not valid */
+#define SPEC_FLAG_TIMEOUT 8u    /* a bulk copy or a wait on other blocks' work did not complete
+                                   within its limit (status word only): outputs of the call are
+                                   not valid and the workspace must be zeroed again */
 
 /* workspace kinds for spec_workspace_bytes */
 #define SPEC_WS_CHAIN 0 /* n = gamma */
@@ -77,6 +78,9 @@ extern "C" {
 #define SPEC_WS_COMMIT 2
 #define SPEC_WS_CHAIN_TOPK 3 /* n = gamma: SPEC_WS_CHAIN plus the candidate pool (32 KiB per
                                 request position) of the fast top-k path (0 < top_k <= 128) */
+#define SPEC_WS_CHAIN_FULL 4 /* n = gamma: SPEC_WS_CHAIN plus the per-slice statistics, draw
+                                state and work queue of the persistent full-vocabulary path
+                                (top_k == 0; about 2 KiB per request position at V = 128,256) */
 
 /*
  * Chain verification, sampled (temperature > 0) or greedy (temperature == 0).
@@ -111,8 +115,16 @@ extern "C" {
  *   for every call.  Sampled calls with 0 < top_k <= 128 take a faster path
  *   (cluster-free candidate lists) when the workspace holds
  *   spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, B, gamma, V) bytes; with less
- *   they take the exact cluster-wide threshold search instead.  Both give
- *   identical results.
+ *   they take the exact cluster-wide threshold search instead.  Sampled calls
+ *   without top-k (and without residual_mass) take a persistent path (one
+ *   cooperative kernel: softmax statistics, decisions and the draw, the draw
+ *   first in fp32 with a certified error bound, in double-float where the
+ *   uniform falls within that bound of a CDF boundary) when the workspace
+ *   holds spec_workspace_bytes(SPEC_WS_CHAIN_FULL, B, gamma, V) bytes, rows
+ *   and strides are 16-byte aligned, V * element size is a multiple of 16,
+ *   gamma <= 30, V * element size <= 1 MiB and the call has at least 1,024
+ *   (row, 4 KiB slice) items; otherwise the cluster kernel.
+ *   All paths give identical results up to the stated tolerances.
  */
 typedef struct SpecChainArgs {
     int32_t B, gamma, V, dtype;
@@ -273,6 +285,14 @@ const char *spec_error_string(int code);
 
 /* Text of the last CUDA error a call of this library saw on this thread. */
 const char *spec_last_cuda_error(void);
+
+/* Diagnostic: the largest relative error of the GPU's hardware exponential
+ * (ex2.approx.ftz.f32) against fp64 over every fp32 input in [-126, 1], on the
+ * current device.  The full-vocabulary path's certified fp32 draw assumes
+ * 1.5e-7; a larger value means that path's certification is not valid on this
+ * device.  Synchronous (about a second of GPU time); SPEC_ERR_CUDA on a CUDA
+ * error. */
+int spec_selftest_ex2(float *max_rel_err);
 
 #ifdef __cplusplus
 }

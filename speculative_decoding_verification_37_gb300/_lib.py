@@ -20,12 +20,12 @@ SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_TOO
 SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
 SPEC_DTYPE_BF16, SPEC_DTYPE_F32 = 0, 1
 SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW, SPEC_FLAG_TIMEOUT = 1, 2, 4, 8
-SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT, SPEC_WS_CHAIN_TOPK = 0, 1, 2, 3
+SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT, SPEC_WS_CHAIN_TOPK, SPEC_WS_CHAIN_FULL = 0, 1, 2, 3, 4
 TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspace holds it
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
             "spec_get_status", "spec_error_string", "spec_last_cuda_error",
-            "spec_verify_chain_static")
+            "spec_verify_chain_static", "spec_selftest_ex2")
 
 
 class SpecChainArgs(ctypes.Structure):
@@ -93,6 +93,8 @@ def lib():
         L.spec_verify_chain_static.restype = c_int
         L.spec_last_cuda_error.argtypes = []
         L.spec_last_cuda_error.restype = c_char_p
+        L.spec_selftest_ex2.argtypes = [POINTER(ctypes.c_float)]
+        L.spec_selftest_ex2.restype = c_int
         _LIB = L
     return _LIB
 
@@ -128,6 +130,14 @@ def new_workspace(kind: int, B: int, n: int, V: int, device="cuda") -> torch.Ten
     """A zero-filled workspace (torch allocates it; the library never does)."""
     nbytes = max(spec_workspace_bytes(kind, B, n, V), 256)
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def spec_selftest_ex2() -> float:
+    """Largest relative error of the GPU's hardware exponential over [-126, 1]
+    (the certified fp32 draw assumes 1.5e-7)."""
+    out = ctypes.c_float(0.0)
+    _check("spec_selftest_ex2", lib().spec_selftest_ex2(ctypes.byref(out)))
+    return float(out.value)
 
 
 def spec_get_status(workspace: torch.Tensor, stream=None) -> int:

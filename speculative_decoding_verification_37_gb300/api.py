@@ -13,11 +13,13 @@ _WORKSPACES: Dict[Tuple, torch.Tensor] = {}
 
 
 def workspace(kind: int, B: int, n: int, V: int, device) -> torch.Tensor:
-    """A cached zero-filled workspace for (device, kind, B, n).  Every call
-    leaves it zeroed, so it is reused without clearing; calls that share it
-    must be ordered on one stream."""
+    """A cached zero-filled workspace for (device, kind, B, n, V) (the size of
+    some kinds depends on V).  Every call leaves it zeroed, so it is reused
+    without clearing; calls that share it must be ordered on one stream."""
     dev = torch.device(device)
-    key = (dev.type, dev.index, kind, B, n)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    key = (dev.type, dev.index, kind, B, n, V)
     ws = _WORKSPACES.get(key)
     if ws is None:
         ws = L.new_workspace(kind, B, n, V, device=dev)
@@ -33,6 +35,17 @@ class ChainOut:
     accept_prob: Optional[torch.Tensor]   # f32 [B, gamma]
     residual_mass: Optional[torch.Tensor] # f32 [B, gamma]
     flags: torch.Tensor                   # uint32 stored as int32 [B]
+
+
+def chain_workspace_kind(sampled: bool, top_k: int, V: int, residual_mass: bool = False) -> int:
+    """The workspace kind that lets a chain call take its fastest path."""
+    if not sampled:
+        return L.SPEC_WS_CHAIN
+    if 0 < top_k <= L.TOPK_FAST_MAX and top_k < V:
+        return L.SPEC_WS_CHAIN_TOPK
+    if (top_k == 0 or top_k >= V) and not residual_mass:
+        return L.SPEC_WS_CHAIN_FULL
+    return L.SPEC_WS_CHAIN
 
 
 def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int,
@@ -57,7 +70,7 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
         if (sampled and residual_mass) else None,
         flags=torch.zeros(B, dtype=torch.int32, device=dev))
     if ws is None:
-        kind = L.SPEC_WS_CHAIN_TOPK if (sampled and 0 < top_k <= L.TOPK_FAST_MAX) else L.SPEC_WS_CHAIN
+        kind = chain_workspace_kind(sampled, top_k, V, residual_mass)
         ws = workspace(kind, B, gamma, V, dev)
     L.spec_verify_chain(target_logits=target, draft_tokens=draft_tokens, n_acc=out.n_acc,
                         out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws, gamma=gamma,

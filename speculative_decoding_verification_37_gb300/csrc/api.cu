@@ -57,6 +57,14 @@ struct Ws {
     void *data;          // chain: records or argmax keys; tree: argmax keys
     uint2 *slicecb;      // chain, top-k: [B*(gamma+1)][2][cmax] (count, bound key)
     uint2 *pool;         // chain, top-k: [B*(gamma+1)][2][cmax][kTopKSlicePool]
+    // chain, full vocabulary: see SampleParams
+    float2 *fpart, *fxd;
+    float4 *fstat;
+    unsigned long long *rstate, *qitem;
+    unsigned *pcnt, *dcnt;
+    DrawRec *drec;
+    DrawPart *dpart;
+    int *amb;
 };
 
 // One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
@@ -65,15 +73,25 @@ struct Ws {
 // count (fp32 rows), so one size serves both element types.
 int topk_slices(int V, int dtype) { return slices_for(V, dtype, 1 << 20, topk_row_bytes()); }
 
+// Slices per row of the full-vocabulary path (sized for fp32 rows, so one
+// size serves both element types).
+int full_slices(int V, int dtype) {
+    return (int)(((int64_t)V * (int64_t)esize(dtype) + full_row_bytes() - 1) / full_row_bytes());
+}
+
+enum WsExtra { kWsPlain = 0, kWsPool = 1, kWsFull = 2 };
+
 // One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
-// (0 for other kinds), `data_bytes` the per-row keys or records; with_pool
-// adds the top-k candidate regions for rows of V logits.
-size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_ptr, bool with_pool,
+// (0 for other kinds), `data_bytes` the per-row keys or records; `extra`
+// adds the top-k candidate regions or the full-vocabulary path's state for
+// rows of V logits.
+size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_ptr, int extra = kWsPlain,
                        int V = 0) {
     char *base = static_cast<char *>(base_ptr);
     size_t off = kWsHeader;
     const size_t per_req = ws_align((size_t)B * sizeof(unsigned));
     if (w) {
+        *w = Ws{};
         w->status = reinterpret_cast<unsigned *>(base);
         w->counters = reinterpret_cast<unsigned *>(base + off);
         w->rejword = reinterpret_cast<unsigned *>(base + off + per_req);
@@ -81,15 +99,44 @@ size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_
     off += 2 * per_req;
     if (w) w->data = base + off;
     off += ws_align(data_bytes);
-    if (!with_pool) {
-        if (w) w->slicecb = nullptr, w->pool = nullptr;
-        return off;
+    auto take = [&](size_t bytes) -> char * {
+        char *at = base ? base + off : nullptr;
+        off += ws_align(bytes);
+        return at;
+    };
+    if (extra == kWsPool) {
+        const size_t cmax = (size_t)topk_slices(V, SPEC_DTYPE_F32);
+        char *cb = take(rows * 2 * cmax * sizeof(uint2));
+        char *pl = take(rows * 2 * cmax * (size_t)kTopKSlicePool * sizeof(uint2));
+        if (w) {
+            w->slicecb = reinterpret_cast<uint2 *>(cb);
+            w->pool = reinterpret_cast<uint2 *>(pl);
+        }
+    } else if (extra == kWsFull) {
+        const size_t c = (size_t)full_slices(V, SPEC_DTYPE_F32), nb = (size_t)B;
+        char *fp = take(rows * 2 * c * sizeof(float2));
+        char *fx = take(rows * sizeof(float2));
+        char *fs = take(rows * sizeof(float4));
+        char *rs = take(nb * sizeof(unsigned long long));
+        char *pc = take(rows * sizeof(unsigned));
+        char *dr = take(nb * sizeof(DrawRec));
+        char *dp = take(nb * c * sizeof(DrawPart));
+        char *dc = take(nb * sizeof(unsigned));
+        char *am = take(nb * c * (size_t)kFullAmb * sizeof(int));
+        char *qi = take(3 * nb * c * sizeof(unsigned long long));
+        if (w) {
+            w->fpart = reinterpret_cast<float2 *>(fp);
+            w->fxd = reinterpret_cast<float2 *>(fx);
+            w->fstat = reinterpret_cast<float4 *>(fs);
+            w->rstate = reinterpret_cast<unsigned long long *>(rs);
+            w->pcnt = reinterpret_cast<unsigned *>(pc);
+            w->drec = reinterpret_cast<DrawRec *>(dr);
+            w->dpart = reinterpret_cast<DrawPart *>(dp);
+            w->dcnt = reinterpret_cast<unsigned *>(dc);
+            w->amb = reinterpret_cast<int *>(am);
+            w->qitem = reinterpret_cast<unsigned long long *>(qi);
+        }
     }
-    const size_t cmax = (size_t)topk_slices(V, SPEC_DTYPE_F32);
-    if (w) w->slicecb = reinterpret_cast<uint2 *>(base + off);
-    off += ws_align(rows * 2 * cmax * sizeof(uint2));
-    if (w) w->pool = reinterpret_cast<uint2 *>(base + off);
-    off += ws_align(rows * 2 * cmax * (size_t)kTopKSlicePool * sizeof(uint2));
     return off;
 }
 
@@ -132,13 +179,14 @@ extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V
     if (B < 0 || n < 0 || V < 0) return 0;
     switch (kind) {
     case SPEC_WS_CHAIN:
-    case SPEC_WS_CHAIN_TOPK: {
+    case SPEC_WS_CHAIN_TOPK:
+    case SPEC_WS_CHAIN_FULL: {
         const size_t rows = (size_t)B * ((size_t)n + 1);
-        return ws_layout_bytes(B, rows, chain_data_bytes(rows), nullptr, nullptr, kind == SPEC_WS_CHAIN_TOPK, V);
+        const int extra = kind == SPEC_WS_CHAIN_TOPK ? kWsPool : kind == SPEC_WS_CHAIN_FULL ? kWsFull : kWsPlain;
+        return ws_layout_bytes(B, rows, chain_data_bytes(rows), nullptr, nullptr, extra, V);
     }
     case SPEC_WS_TREE:
-        return ws_layout_bytes(B, 0, (size_t)B * (size_t)n * sizeof(unsigned long long), nullptr, nullptr,
-                               false);
+        return ws_layout_bytes(B, 0, (size_t)B * (size_t)n * sizeof(unsigned long long), nullptr, nullptr);
     case SPEC_WS_COMMIT:
         return kWsHeader + ws_align((size_t)B * sizeof(unsigned));
     default:
@@ -170,9 +218,14 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     if (!workspace || !aligned(workspace, 256) ||
         ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
         return SPEC_ERR_INVALID_ARG;
-    const bool has_pool = ws_bytes >= spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, a->B, a->gamma, a->V);
+    // the extra regions a larger workspace holds (the kinds never both fit the
+    // same size test by accident: each is checked against its own size)
+    const bool sampled_full = !greedy && (a->top_k == 0 || a->top_k >= a->V);
+    const bool has_full = sampled_full && ws_bytes >= spec_workspace_bytes(SPEC_WS_CHAIN_FULL, a->B, a->gamma, a->V);
+    const bool has_pool = !has_full && ws_bytes >= spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, a->B, a->gamma, a->V);
     Ws w;
-    ws_layout_bytes(a->B, (size_t)rows, chain_data_bytes((size_t)rows), &w, workspace, has_pool, a->V);
+    ws_layout_bytes(a->B, (size_t)rows, chain_data_bytes((size_t)rows), &w, workspace,
+                    has_full ? kWsFull : has_pool ? kWsPool : kWsPlain, a->V);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (greedy) {
@@ -210,6 +263,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.unif = a->uniforms;
         const double c2 = 1.4426950408889634074 / (double)a->temperature;
         p.c2 = (float)c2;
+        p.c2lo = (float)(c2 - (double)p.c2);
         p.exptab = exp_tables();
         split(1.0 / (double)a->temperature, p.exptab.it);
         p.top_k = (a->top_k >= a->V) ? 0 : a->top_k;
@@ -226,7 +280,37 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.recs = static_cast<PosRec *>(w.data);
         p.slicecb = w.slicecb;
         p.pool = w.pool;
+        p.fpart = w.fpart;
+        p.fxd = w.fxd;
+        p.fstat = w.fstat;
+        p.rstate = w.rstate;
+        p.pcnt = w.pcnt;
+        p.drec = w.drec;
+        p.dpart = w.dpart;
+        p.dcnt = w.dcnt;
+        p.amb = w.amb;
+        p.qitem = w.qitem;
+        p.qcap = (unsigned)(3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32));
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
+        // full vocabulary: the persistent kernel when the workspace, the
+        // rows' alignment and the sizes allow it
+        const int64_t rbytes = (int64_t)a->V * (int64_t)es;
+        // (small calls stay on the cluster kernel: a whole-GPU cooperative
+        // grid only pays off with a few thousand slices of work)
+        const bool full = has_full && p.top_k == 0 && !a->residual_mass && a->gamma <= 30 &&
+                          rows * full_slices(a->V, a->dtype) >= 1024 &&
+                          rbytes % 16 == 0 && rbytes <= (int64_t)full_row_bytes() * full_max_slices() &&
+                          aligned(a->target_logits, 16) && (a->target_row_stride * (int64_t)es) % 16 == 0 &&
+                          (a->gamma == 0 || (aligned(a->draft_logits, 16) &&
+                                             (a->draft_row_stride * (int64_t)es) % 16 == 0));
+        if (full) {
+            p.c = full_slices(a->V, a->dtype);
+            p.Vs = full_row_bytes() / (int)es;
+            if (rows * p.c > 0x7fffffffLL / 3 || 3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32) > 0x7fffffffLL)
+                return SPEC_ERR_UNSUPPORTED;
+            e = launch_chain_full(p, a->dtype, sm_count(), s);
+            return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+        }
         // top-k <= 128: cluster-free candidate lists when every slice's share
         // (about k + a few) fits the per-position pool; otherwise the cluster
         // kernel with its exact threshold search
@@ -262,7 +346,7 @@ extern "C" int spec_verify_tree(const SpecTreeArgs *a, void *workspace, size_t w
         return SPEC_ERR_INVALID_ARG;
     const int64_t rows = (int64_t)a->B * a->R;
     Ws w;
-    ws_layout_bytes(a->B, 0, (size_t)rows * sizeof(unsigned long long), &w, workspace, false);
+    ws_layout_bytes(a->B, 0, (size_t)rows * sizeof(unsigned long long), &w, workspace);
     ArgmaxParams p = {};
     p.rows = a->logits;
     p.stride = a->row_stride;

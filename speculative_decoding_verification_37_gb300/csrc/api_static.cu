@@ -58,5 +58,7 @@ extern "C" int spec_verify_chain_static(const SpecChainArgs *a, void *stream) {
     const size_t zeroed = specv::kWsHeader + 2 * specv::ws_align((size_t)a->B * sizeof(unsigned));
     e = cudaMemsetAsync(g_ws_ptr[dev], 0, zeroed, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    return spec_verify_chain(a, g_ws_ptr[dev], kStaticWsBytes, stream);
+    // the plain chain workspace only: the candidate regions and the
+    // full-vocabulary path's state are not part of this array's contract
+    return spec_verify_chain(a, g_ws_ptr[dev], need, stream);
 }

@@ -45,6 +45,18 @@ struct ArgmaxParams {
 
 constexpr int kTopKFastMax = 128;  // top_k served by the candidate-list path
 
+// Full-vocabulary persistent path (verify_full.cu): a request's draw record
+// and one (request, slice) result of a draw round.
+struct DrawRec {
+    int kstar, mode, pass, pad;  // mode 0: residual of position kstar, 1: bonus row
+    float4 inv;                  // round 2: 1/S_p and 1/S_q as dd pairs
+};
+struct alignas(16) DrawPart {  // copied with 16-byte vector loads and stores
+    float v[12];
+    unsigned namb, pad[3];
+};
+constexpr int kFullAmb = 16;  // in-band residual elements listed per (request, slice)
+
 struct SampleParams {
     int B, gamma, V, c, Vs;
     const void *target;
@@ -54,6 +66,7 @@ struct SampleParams {
     const int *tokens;
     const float *unif;
     float c2;      // log2(e) / temperature
+    float c2lo;    // its rounding residue: c2 + c2lo = log2(e) / temperature to ~2^-48
     DdExpTables exptab;   // 1/T, ln2/64 in parts, 2^(j/64): the double-float exponential
     int top_k;     // 0 = keep all
     float eps;
@@ -68,6 +81,18 @@ struct SampleParams {
     // entries, slice stride c
     uint2 *slicecb;      // [B*(gamma+1)][2][c]
     uint2 *pool;         // [B*(gamma+1)][2][c][kTopKSlicePool]
+    // full-vocabulary persistent path, c = slices of full_row_bytes()
+    float2 *fpart;               // [B*(gamma+1)][2][c] (max, sum) per slice
+    float2 *fxd;                 // [B*(gamma+1)] target and draft logit at the draft token
+    float4 *fstat;               // [B*(gamma+1)] (M_p, S_p, M_q, S_q)
+    unsigned long long *rstate;  // [B] decided / stop bits per position
+    unsigned *pcnt;              // [B*(gamma+1)] slice arrivals
+    DrawRec *drec;               // [B]
+    DrawPart *dpart;             // [B][c]
+    unsigned *dcnt;              // [B] draw-round arrivals
+    int *amb;                    // [B][c][kFullAmb]
+    unsigned long long *qitem;   // [qcap] queue slots
+    unsigned qcap;               // 3*B*(slices the workspace was sized for)
 };
 
 constexpr int kTopKSlicePool = 256;  // candidates one slice of one row may hand on
@@ -88,6 +113,9 @@ cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, i
 int argmax_stage_bytes();  // a greedy slice body must fit this
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s);
+cudaError_t launch_chain_full(const SampleParams &p, int dtype, int sms, cudaStream_t s);
+int full_row_bytes();   // one row's slice of the full-vocabulary path
+int full_max_slices();  // slices per row it supports
 int topk_row_bytes();  // a top-k slice body per row must fit this
 struct CommitGeom {
     int ppu, upp, groups;

@@ -107,6 +107,12 @@ __device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t 
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// asynchronous prefetch of `bytes` (multiple of 16, address 16-byte aligned)
+// into L2; no completion to wait for
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 // waits until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
