@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(32) commit_kv_kernel(CommitParams p) {
     const bool head = i == 0 && grp == 0;
 
     const int n = p.n_slots[b];
+    const int len0 = p.len[b];  // loaded with n: one round trip
     if (!head && (unsigned)i >= (unsigned)n) return;  // past n_slots (or n < 0: the head flags it)
-    const int len0 = p.len[b];
     bool good = n >= 0 && n <= S && len0 >= 0 && (int64_t)len0 + n <= (int64_t)p.max_blocks * p.bs;
     bool lane_ok = true;
     int slot_i = 0, blk_i = 0;
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(32) commit_kv_kernel(CommitParams p) {
             so += bytes;
         }
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read();  // the stage may go; the writes finish before the kernel does
     } else {
         // the loads are still outstanding: give them one more bounded wait
         // before the block (and its shared memory) goes away
@@ -138,8 +138,9 @@ __global__ void __launch_bounds__(32) commit_kv_kernel(CommitParams p) {
     }
     mbar_inval(&bar);
 
-    // the last block of the request advances its length
-    __threadfence();
+    // the last block of the request advances its length (every block of the
+    // request read the old length before it arrived; nothing in this kernel
+    // reads it after, so the arrival need not wait for the writes)
     if (atomicAdd(p.counters + b, 1u) == (unsigned)(n * G - 1)) {
         __threadfence();
         const int nl = len0 + n;

@@ -116,6 +116,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t byte
 // waits until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// waits until every committed bulk store of this thread has read its shared
+// memory source (the writes to global memory may still be in flight; they
+// complete before the kernel does)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Ring of NST stages x ROWS rows x CH bytes.
 template <int CH, int NST, int ROWS> struct Ring {
     alignas(128) unsigned char buf[NST][ROWS][CH];
