@@ -7,3 +7,4 @@ CUDA library and is never on the product path.
 from .spec_oracle import *  # noqa: F401,F403
 from .spec_oracle import (BOUNDARY_MARGIN, DEFAULT_EPS, FLAG_BAD_INPUT, FLAG_BAD_ROW,  # noqa: F401
                           FLAG_FALLBACK)
+from .ngram_oracle import NgramDraft, ngram_draft  # noqa: F401
