@@ -447,6 +447,113 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+NGRAM_METRIC = "n-gram drafts: requests/s + history GB/s vs peak"
+
+
+def run_ngram(args, rank, world, local):
+    """The prompt-lookup drafter on a batch of long histories (one launch per
+    step, histories resident; L2 flushed between steps)."""
+    spec = W.NGRAM_SPEC
+    hist, lens = W.make_histories(spec, seed=rank)
+    hist_bytes = int(lens.astype(np.int64).sum()) * 4
+    cfg = {"workload": spec.name, "B_per_gpu": spec.B, "max_len": spec.max_len, "V": spec.vocab,
+           "gamma": spec.gamma, "n_min": spec.n_min, "n_max": spec.n_max,
+           "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+           "parallelism": f"dp{world} (independent request shards, no collective)"}
+    if args.impl == "reference":
+        if rank == 0:
+            v, sample = ngram_oracle_sample(hist, lens, spec, seconds=max(2.0, 2.0 * args.steps))
+            print(json.dumps({"impl": "reference", "metric": NGRAM_METRIC, "value": v, "unit": "requests/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+                              "data": "synthetic", "config": cfg,
+                              "cpu_baseline": {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                                               "sample": sample},
+                              "e2e": {"value": v, "unit": "requests/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    from speculative_decoding_verification_37_gb300 import build as _b
+    from speculative_decoding_verification_37_gb300 import api
+    _b.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d_hist = torch.from_numpy(hist).to(dev)
+    d_lens = torch.from_numpy(lens).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    run = lambda h, l: api.ngram_draft(h, l, gamma=spec.gamma, n_min=spec.n_min, n_max=spec.n_max)
+    for _ in range(max(3, args.warmup)):
+        run(d_hist, d_lens)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier(world)
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run(d_hist, d_lens)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    barrier(world)
+    clk = clocks.stop()
+    t = max_over_ranks(statistics.mean(times), world)
+    peak, peak_kind = measured_peaks()
+    achieved = hist_bytes / (t * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        h_hist, h_lens = torch.from_numpy(hist).pin_memory(), torch.from_numpy(lens).pin_memory()
+        et = []
+        for i in range(5):
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            d_hist.copy_(h_hist, non_blocking=True)
+            d_lens.copy_(h_lens, non_blocking=True)
+            o = run(d_hist, d_lens)
+            host = [o.draft_tokens.to("cpu", non_blocking=True), o.n_draft.to("cpu", non_blocking=True)]
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                et.append(e0.elapsed_time(e1))
+        te = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": spec.B * world / (te * 1e-3), "unit": "requests/s",
+               "h2d_bytes_per_step": hist.nbytes + lens.nbytes,
+               "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+               "ms_per_step": round(te, 4)}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample = ngram_oracle_sample(hist, lens, spec, seconds=8.0)
+        cpu = {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({"metric": NGRAM_METRIC, "value": spec.B * world / (t * 1e-3), "unit": "requests/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 5),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+                          "data": "synthetic", "config": cfg,
+                          "roofline": {"bound": "hbm", "kernel": "ngram_draft_kernel", "achieved": round(achieved, 1),
+                                       "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                                       "traffic": None, "algorithmic_bytes": hist_bytes,
+                                       "avg_launch_ms": round(t, 5),
+                                       "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+                          "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+                          "kernel_source": kernel_source_hash()}), flush=True)
+
+
+def ngram_oracle_sample(hist, lens, spec, seconds: float):
+    """Times the oracle on this host, one request at a time over the batch's
+    first requests, for about `seconds`."""
+    import oracle as O
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds and n < spec.B:
+        O.ngram_draft(hist[n, :lens[n]].tolist(), spec.n_min, spec.n_max, spec.gamma)
+        n += 1
+    el = time.perf_counter() - t0
+    return n / el, f"{n} requests of the batch (histories of up to {spec.max_len} tokens), {el:.1f} s on one core"
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,8 +565,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's request count (smaller cases for profiling)")
+    ap.add_argument("--workload", default="verify", choices=["verify", "ngram"],
+                    help="ngram: the prompt-lookup drafter on long token histories instead")
     args = ap.parse_args()
     rank, world, local = dist_setup()
+    if args.workload == "ngram":
+        run_ngram(args, rank, world, local)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
@@ -583,7 +695,7 @@ def main():
                 "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /
                                   (t_step_max * 1e-3) / 1e9, 1),
                 "roofline": roofline, "commit": commit, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * (2 if wl.kvb is not None else 1),
+                "gpu_launches": args.steps * ((2 if "+" in kname else 1) + (1 if wl.kvb is not None else 0)),
                 "clocks": clk, "kernel_source": kernel_source_hash()}
         print(json.dumps(line), flush=True)
     if world > 1:

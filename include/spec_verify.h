@@ -286,6 +286,40 @@ const char *spec_error_string(int code);
 /* Text of the last CUDA error a call of this library saw on this thread. */
 const char *spec_last_cuda_error(void);
 
+/*
+ * N-gram (prompt-lookup) drafts, a model-free draft source ("10.6 投机解码"
+ * §10.6.3 实际部署; "KV Cache 优化（四）" §10.2 N-gram 或前缀匹配): for each
+ * request, the longest n in [n_min, n_max] whose trailing n-gram of the
+ * history occurs earlier (an occurrence starting before the trailing n-gram
+ * itself), the most recent such occurrence, and the up to gamma tokens that
+ * follow it (never past the end of the history).  No occurrence gives an
+ * empty draft.
+ *
+ * history: device int32; request b's tokens start at history + b *
+ *   history_stride, hist_len[b] of them (0 <= hist_len[b] <= history_stride).
+ * Outputs (device): draft_tokens[b][0..gamma) (row stride gamma; entries past
+ *   n_draft[b] are -1), n_draft[b]; optional (NULL = not written): match_n[b]
+ *   (the n used, 0 if none), match_start[b] (-1 if none), flags[b].
+ * Errors: SPEC_ERR_INVALID_ARG for B < 0, gamma < 0, n_min < 1,
+ *   n_max < n_min, n_max > 64, history_stride < 1 or a NULL required pointer
+ *   (nothing is launched); a hist_len[b] outside [0, history_stride] gives
+ *   n_draft[b] = 0, SPEC_FLAG_BAD_INPUT in flags[b] (if given), and that
+ *   request only is skipped.  Asynchronous on `stream`; no workspace.
+ */
+typedef struct SpecNgramArgs {
+    int32_t B, gamma, n_min, n_max;
+    const int32_t *history;     /* device, int32 [B][history_stride] */
+    int64_t history_stride;     /* elements */
+    const int32_t *hist_len;    /* device, int32 [B] */
+    int32_t *draft_tokens;      /* device out [B][gamma] */
+    int32_t *n_draft;           /* device out [B] */
+    int32_t *match_n;           /* device out [B] or NULL */
+    int32_t *match_start;       /* device out [B] or NULL */
+    uint32_t *flags;            /* device out [B] or NULL */
+} SpecNgramArgs;
+
+int spec_ngram_draft(const SpecNgramArgs *args, void *stream);
+
 /* Diagnostic: the largest relative error of the GPU's hardware exponential
  * (ex2.approx.ftz.f32) against fp64 over every fp32 input in [-126, 1], on the
  * current device.  The full-vocabulary path's certified fp32 draw assumes

@@ -5,6 +5,6 @@ from ._lib import (EXPORTED, SPEC_DTYPE_BF16, SPEC_DTYPE_F32, SPEC_ERR_CUDA,  # 
                    SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_FLAG_BAD_INPUT,
                    SPEC_FLAG_BAD_ROW, SPEC_FLAG_FALLBACK, SPEC_FLAG_TIMEOUT, SPEC_OK, SPEC_WS_CHAIN,
                    SPEC_WS_CHAIN_FULL, SPEC_WS_CHAIN_TOPK, SPEC_WS_COMMIT,
-                   SPEC_WS_TREE, SpecError, lib, new_workspace, spec_commit_kv, spec_get_status,
+                   SPEC_WS_TREE, SpecError, lib, new_workspace, spec_commit_kv, spec_get_status, spec_ngram_draft,
                    spec_verify_chain, spec_verify_tree, spec_workspace_bytes)
-from .api import ChainOut, TreeOut, chain_workspace_kind, commit_kv, verify_chain, verify_tree, workspace  # noqa: F401
+from .api import ChainOut, NgramOut, TreeOut, chain_workspace_kind, commit_kv, ngram_draft, verify_chain, verify_tree, workspace  # noqa: F401

@@ -25,7 +25,7 @@ TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspa
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
             "spec_get_status", "spec_error_string", "spec_last_cuda_error",
-            "spec_verify_chain_static", "spec_selftest_ex2")
+            "spec_verify_chain_static", "spec_selftest_ex2", "spec_ngram_draft")
 
 
 class SpecChainArgs(ctypes.Structure):
@@ -56,6 +56,13 @@ class SpecCommitArgs(ctypes.Structure):
                 ("slots", c_void_p), ("slots_stride", c_int32),
                 ("n_slots", c_void_p), ("committed_len", c_void_p),
                 ("blocks_in_use", c_void_p), ("flags", c_void_p)]
+
+
+class SpecNgramArgs(ctypes.Structure):
+    _fields_ = [("B", c_int32), ("gamma", c_int32), ("n_min", c_int32), ("n_max", c_int32),
+                ("history", c_void_p), ("history_stride", c_int64), ("hist_len", c_void_p),
+                ("draft_tokens", c_void_p), ("n_draft", c_void_p), ("match_n", c_void_p),
+                ("match_start", c_void_p), ("flags", c_void_p)]
 
 
 class SpecError(RuntimeError):
@@ -95,6 +102,8 @@ def lib():
         L.spec_last_cuda_error.restype = c_char_p
         L.spec_selftest_ex2.argtypes = [POINTER(ctypes.c_float)]
         L.spec_selftest_ex2.restype = c_int
+        L.spec_ngram_draft.argtypes = [POINTER(SpecNgramArgs), c_void_p]
+        L.spec_ngram_draft.restype = c_int
         _LIB = L
     return _LIB
 
@@ -130,6 +139,19 @@ def new_workspace(kind: int, B: int, n: int, V: int, device="cuda") -> torch.Ten
     """A zero-filled workspace (torch allocates it; the library never does)."""
     nbytes = max(spec_workspace_bytes(kind, B, n, V), 256)
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def spec_ngram_draft(*, history: torch.Tensor, hist_len: torch.Tensor, gamma: int, n_min: int,
+                     n_max: int, draft_tokens: torch.Tensor, n_draft: torch.Tensor,
+                     match_n: Optional[torch.Tensor] = None, match_start: Optional[torch.Tensor] = None,
+                     flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Marshals one spec_ngram_draft call: history int32 [B, stride] (rows may
+    be strided), hist_len int32 [B], draft_tokens int32 [B, gamma]."""
+    a = SpecNgramArgs(B=history.shape[0], gamma=gamma, n_min=n_min, n_max=n_max, history=_ptr(history),
+                      history_stride=history.stride(0), hist_len=_ptr(hist_len),
+                      draft_tokens=_ptr(draft_tokens), n_draft=_ptr(n_draft), match_n=_ptr(match_n),
+                      match_start=_ptr(match_start), flags=_ptr(flags))
+    _check("spec_ngram_draft", lib().spec_ngram_draft(ctypes.byref(a), _stream(stream)))
 
 
 def spec_selftest_ex2() -> float:

@@ -129,3 +129,28 @@ def commit_kv(temp_kv: torch.Tensor, cache: torch.Tensor, block_table: torch.Ten
     L.spec_commit_kv(temp_kv=temp_kv, cache=cache, block_table=block_table, n_slots=n_slots,
                      committed_len=committed_len, block_size=block_size, workspace=ws,
                      slots=slots, blocks_in_use=blocks_in_use, flags=flags, stream=stream)
+
+
+@dataclass
+class NgramOut:
+    draft_tokens: torch.Tensor   # int32 [B, gamma], -1 past n_draft
+    n_draft: torch.Tensor        # int32 [B]
+    match_n: torch.Tensor        # int32 [B], 0 if no match
+    match_start: torch.Tensor    # int32 [B], -1 if no match
+    flags: torch.Tensor          # int32 [B]
+
+
+def ngram_draft(history: torch.Tensor, hist_len: torch.Tensor, *, gamma: int, n_min: int = 1,
+                n_max: int = 4, stream=None) -> NgramOut:
+    """Prompt-lookup drafts: history int32 [B, max_len] on the device (row b's
+    first hist_len[b] tokens are its history)."""
+    dev = history.device
+    B = history.shape[0]
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = NgramOut(draft_tokens=torch.empty((B, gamma), **i32), n_draft=torch.empty(B, **i32),
+                   match_n=torch.empty(B, **i32), match_start=torch.empty(B, **i32),
+                   flags=torch.empty(B, **i32))
+    L.spec_ngram_draft(history=history, hist_len=hist_len, gamma=gamma, n_min=n_min, n_max=n_max,
+                       draft_tokens=out.draft_tokens, n_draft=out.n_draft, match_n=out.match_n,
+                       match_start=out.match_start, flags=out.flags, stream=stream)
+    return out

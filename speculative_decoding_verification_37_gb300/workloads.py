@@ -414,3 +414,55 @@ __all__ = [
     "grow_tree", "TreeBatch", "make_tree", "KVBatch", "make_kv", "make_cache",
     "uniforms24", "KV_SENTINEL",
 ]
+
+
+# --------------------------------------------------------------------------
+# token histories for the n-gram (prompt-lookup) drafter
+# --------------------------------------------------------------------------
+@dataclass
+class HistorySpec:
+    name: str
+    B: int
+    max_len: int
+    vocab: int
+    gamma: int
+    n_min: int
+    n_max: int
+    copy_frac: float = 0.5   # share of segments copied from earlier in the history
+
+
+# A large batch of long histories (an HBM scan of about 134 MB); the shapes
+# follow the chain workloads' vocabulary and the framework's default prompt
+# lookup window.
+NGRAM_SPEC = HistorySpec("ngram B=1024 L<=32768 V=128256 n=1..4 g=8", B=1024, max_len=32768,
+                         vocab=128256, gamma=8, n_min=1, n_max=4)
+
+
+def make_histories(spec: HistorySpec, seed: int = 0, requests: Optional[Sequence[int]] = None):
+    """Returns (history int32 [n, max_len] padded with -1, lengths int32 [n]).
+    A history is a sequence of segments: a copy (probability copy_frac) of an
+    earlier stretch of 4..64 tokens, so that n-grams recur, or 4..64 fresh
+    tokens drawn uniformly from the vocabulary; the last segment is always a
+    copy (the text being generated continues a passage seen before, the case
+    prompt lookup serves).  Lengths are drawn in [max_len/2, max_len]."""
+    idx = list(range(spec.B)) if requests is None else list(requests)
+    hist = np.full((len(idx), spec.max_len), -1, dtype=np.int32)
+    lens = np.zeros(len(idx), dtype=np.int32)
+    for r, b in enumerate(idx):
+        rng = _rng(seed, 9, b)
+        L = int(rng.integers(spec.max_len // 2, spec.max_len + 1))
+        h = np.empty(L, dtype=np.int32)
+        at = 0
+        while at < L:
+            m = int(min(rng.integers(4, 65), L - at))
+            last = at + m >= L
+            if at >= 8 and (last or rng.random() < spec.copy_frac):
+                src = int(rng.integers(0, at - min(m, at) + 1))
+                m = min(m, at - src)
+                h[at:at + m] = h[src:src + m]
+            else:
+                h[at:at + m] = rng.integers(0, spec.vocab, size=m, dtype=np.int32)
+            at += m
+        hist[r, :L] = h
+        lens[r] = L
+    return hist, lens
