@@ -226,16 +226,23 @@ def run_step(wl: Workload, inp, events=None, ws=None):
 class Step:
     """The timed step with every output and workspace preallocated, the
     verify call and the commit call each captured in a CUDA graph so that
-    the timed region holds GPU work only (no allocation, no host latency)."""
+    the timed region holds GPU work only (no allocation, no host latency).
+    With ``in_place`` (chain only) the candidates' K/V are taken as written
+    in place by the target forward: the verify call advances the lengths
+    itself and there is no commit launch."""
 
-    def __init__(self, wl: Workload):
+    def __init__(self, wl: Workload, in_place: bool = False):
         from speculative_decoding_verification_37_gb300 import _lib as L
         from speculative_decoding_verification_37_gb300 import api
         self.wl = wl
+        self.in_place = in_place
         s, dev, inp = wl.spec, wl.device, wl.inputs
         i32 = dict(dtype=torch.int32, device=dev)
         B = wl.B
         if wl.kind == "tree":
+            if in_place:
+                raise SystemExit("--kv-commit inplace applies to chain workloads (a tree's kept "
+                                 "path is not a contiguous run of its candidates)")
             N, R = s.n_nodes, s.n_rows
             W_ = (N + 1 + 31) // 32
             self.out = dict(path=torch.empty((B, N), **i32), n_acc=torch.empty(B, **i32),
@@ -256,16 +263,26 @@ class Step:
                             n_out=torch.empty(B, **i32), flags=torch.empty(B, **i32))
             kind = api.chain_workspace_kind(not s.greedy, s.top_k, s.V)
             self.ws = L.new_workspace(kind, B, g, s.V, dev)
+            ip = {}
+            if in_place:
+                if wl.kvb is None:
+                    raise SystemExit("--kv-commit inplace needs a workload with a KV cache")
+                bs = wl.kvb.kv.block_size
+                self.dlen0 = wl.len0 + g
+                self.draft_len = self.dlen0.clone()
+                ip = dict(committed_len=inp["committed_len"], draft_len=self.draft_len,
+                          blocks_in_use=torch.empty(B, **i32), block_size=bs,
+                          kv_capacity=wl.kvb.max_blocks * bs)
 
             def verify():
                 L.spec_verify_chain(target_logits=inp["target"], draft_tokens=inp["draft_tokens"],
                                     workspace=self.ws, gamma=g, temperature=s.temperature,
                                     draft_logits=inp.get("draft"), uniforms=inp.get("uniforms"),
-                                    top_k=s.top_k, **self.out)
+                                    top_k=s.top_k, **self.out, **ip)
             self.n_slots, self.slots = self.out["n_out"], None
         self.verify = verify
         self.commit = None
-        if wl.kvb is not None:
+        if wl.kvb is not None and not in_place:
             self.cws = L.new_workspace(L.SPEC_WS_COMMIT, B, 0, 0, dev)
 
             def commit():
@@ -278,6 +295,8 @@ class Step:
     def reset(self):
         if self.wl.kvb is not None:
             self.wl.inputs["committed_len"].copy_(self.wl.len0)
+        if self.in_place:
+            self.draft_len.copy_(self.dlen0)
 
     def eager(self):
         self.reset()
@@ -567,6 +586,9 @@ def main():
                     help="override the workload's request count (smaller cases for profiling)")
     ap.add_argument("--workload", default="verify", choices=["verify", "ngram"],
                     help="ngram: the prompt-lookup drafter on long token histories instead")
+    ap.add_argument("--kv-commit", default="copy", choices=["copy", "inplace"],
+                    help="inplace (chain): K/V written in place by the forward, the verify "
+                         "call advances the lengths, no commit kernel")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     if args.workload == "ngram":
@@ -585,7 +607,8 @@ def main():
     torch.cuda.set_device(dev)
     wl = Workload(args.config, seed=rank, device=dev, batch=args.batch)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    step = Step(wl)
+    in_place = args.kv_commit == "inplace"
+    step = Step(wl, in_place=in_place)
     step.capture()
 
     # warm-up
@@ -639,7 +662,11 @@ def main():
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s"}
     commit = None
-    if wl.kvb is not None:
+    if in_place:
+        commit = {"kernel": None, "mode": "in place: the verify call advances committed_len, "
+                  "draft_len and blocks_in_use; no K/V copy, no commit launch",
+                  "committed_tokens": n_commit_total}
+    elif wl.kvb is not None:
         t_commit = statistics.mean(commit_ms)
         kvb = kv_bytes(wl, n_commit_total)
         ctr = traffic_record("commit_kv_kernel", config_dict(args.config, world, args.batch)["workload"])
@@ -695,8 +722,11 @@ def main():
                 "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /
                                   (t_step_max * 1e-3) / 1e9, 1),
                 "roofline": roofline, "commit": commit, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * ((2 if "+" in kname else 1) + (1 if wl.kvb is not None else 0)),
+                "gpu_launches": args.steps * ((2 if "+" in kname else 1) +
+                                              (1 if wl.kvb is not None and not in_place else 0)),
                 "clocks": clk, "kernel_source": kernel_source_hash()}
+        if in_place:
+            line["config"]["kv_commit"] = "in place (length advance inside the verify call)"
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -143,6 +143,30 @@ typedef struct SpecChainArgs {
     float *accept_prob;         /* device out [B][gamma] or NULL */
     float *residual_mass;       /* device out [B][gamma] or NULL */
     uint32_t *flags;            /* device out [B] or NULL */
+    /* In-place KV commit ("KV Cache 优化（四）" §6: reserved slots and a
+     * commit-length pointer; "10.6 投机解码" §10.6.3: the gamma+1 positions'
+     * K/V are in the cache before the verify, the cache length is cut back
+     * past a rejection, the draft model's cache rolls back with it).  When
+     * committed_len is given, the target forward has written the K/V of the
+     * gamma+1 candidates (the last emitted token, then the drafts) at cache
+     * positions committed_len[b] .. committed_len[b]+gamma, and this call
+     * commits them itself, with no copy and no extra launch:
+     *   committed_len[b] += n_out[b]   (that token and the accepted drafts;
+     *                                   the rejected ones lie past the new
+     *                                   boundary and are simply not kept)
+     *   draft_len[b] = min(draft_len[b], committed_len[b])   (the draft
+     *                                   cache's length, cut back to the same
+     *                                   boundary, never raised)
+     *   blocks_in_use[b] = ceil(committed_len[b] / block_size)
+     * A request with committed_len[b] < 0, or whose gamma+1 reserved
+     * positions pass kv_capacity (> 0) or 2^31-1, is flagged
+     * SPEC_FLAG_BAD_INPUT (n_out 0).  A flagged request keeps all three
+     * values as they were. */
+    int32_t *committed_len;     /* device in/out [B] or NULL (then the rest is ignored) */
+    int32_t *draft_len;         /* device in/out [B] or NULL */
+    int32_t *blocks_in_use;     /* device out [B] or NULL (needs block_size >= 1) */
+    int32_t block_size;         /* tokens per cache block, for blocks_in_use */
+    int64_t kv_capacity;        /* positions a request's block table covers; 0 = unchecked */
 } SpecChainArgs;
 
 int spec_verify_chain(const SpecChainArgs *args, void *workspace, size_t workspace_bytes,

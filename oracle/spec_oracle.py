@@ -382,3 +382,35 @@ def blocks_in_use(length: int, block_size: int) -> int:
     """Blocks a request of this length occupies; blocks past it may be freed
     by the caller ([LLMI §10.6.3]: paged caches release the surplus)."""
     return -(-length // block_size)
+
+
+@dataclass
+class InPlaceCommit:
+    committed_len: int
+    draft_len: Optional[int]      # None: not tracked
+    blocks_in_use: Optional[int]  # None: left as it was (a flagged request)
+    flags: int
+
+
+def commit_in_place(committed_len: int, n_out: int, gamma: int, block_size: int,
+                    draft_len: Optional[int] = None, kv_capacity: int = 0) -> InPlaceCommit:
+    """Commit of a chain round whose candidates' K/V the target forward
+    already wrote in place, at positions committed_len .. committed_len+gamma
+    ([KV4 §6]: reserved slots and a commit-length pointer, no copy;
+    [LLMI §10.6.3]: those gamma+1 positions are in the cache before the
+    verify, the length is cut back past a rejection, the draft model's cache
+    rolls back with it).
+
+    The kept positions are the last emitted token and the accepted drafts,
+    i.e. the first n_out candidates; the length moves past them and the
+    rejected ones stay beyond it.  The draft cache's length is cut back to the
+    same boundary and never raised (reading: with every draft accepted the
+    draft model has not yet run on the last one).  A request whose reserved
+    positions do not fit (a negative length, or past kv_capacity > 0 or
+    2^31-1) is flagged FLAG_BAD_INPUT and keeps every length."""
+    end = committed_len + gamma + 1
+    if committed_len < 0 or end > 2**31 - 1 or (kv_capacity > 0 and end > kv_capacity):
+        return InPlaceCommit(committed_len, draft_len, None, FLAG_BAD_INPUT)
+    new_len = committed_len + n_out
+    dl = None if draft_len is None else min(draft_len, new_len)
+    return InPlaceCommit(new_len, dl, blocks_in_use(new_len, block_size), 0)

@@ -35,7 +35,9 @@ class SpecChainArgs(ctypes.Structure):
                 ("draft_tokens", c_void_p), ("uniforms", c_void_p),
                 ("temperature", c_float), ("top_k", c_int32), ("fallback_eps", c_float),
                 ("n_acc", c_void_p), ("out_tokens", c_void_p), ("n_out", c_void_p),
-                ("accept_prob", c_void_p), ("residual_mass", c_void_p), ("flags", c_void_p)]
+                ("accept_prob", c_void_p), ("residual_mass", c_void_p), ("flags", c_void_p),
+                ("committed_len", c_void_p), ("draft_len", c_void_p), ("blocks_in_use", c_void_p),
+                ("block_size", c_int32), ("kv_capacity", c_int64)]
 
 
 class SpecTreeArgs(ctypes.Structure):
@@ -175,7 +177,11 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       uniforms: Optional[torch.Tensor] = None, top_k: int = 0,
                       fallback_eps: float = 1e-6, accept_prob: Optional[torch.Tensor] = None,
                       residual_mass: Optional[torch.Tensor] = None,
-                      flags: Optional[torch.Tensor] = None, stream=None) -> None:
+                      flags: Optional[torch.Tensor] = None,
+                      committed_len: Optional[torch.Tensor] = None,
+                      draft_len: Optional[torch.Tensor] = None,
+                      blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
+                      kv_capacity: int = 0, stream=None) -> None:
     """Marshals one spec_verify_chain call.  Logits are 2-D [rows, V] views
     (row stride = stride(0)); every tensor must already be on the device."""
     V = target_logits.shape[-1]
@@ -189,7 +195,9 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       fallback_eps=float(fallback_eps), n_acc=_ptr(n_acc),
                       out_tokens=_ptr(out_tokens), n_out=_ptr(n_out),
                       accept_prob=_ptr(accept_prob), residual_mass=_ptr(residual_mass),
-                      flags=_ptr(flags))
+                      flags=_ptr(flags), committed_len=_ptr(committed_len),
+                      draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
+                      block_size=int(block_size), kv_capacity=int(kv_capacity))
     _check("spec_verify_chain", lib().spec_verify_chain(
         ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream)))
 
@@ -241,7 +249,11 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                              uniforms: Optional[torch.Tensor] = None, top_k: int = 0,
                              fallback_eps: float = 1e-6, accept_prob: Optional[torch.Tensor] = None,
                              residual_mass: Optional[torch.Tensor] = None,
-                             flags: Optional[torch.Tensor] = None, stream=None) -> None:
+                             flags: Optional[torch.Tensor] = None,
+                             committed_len: Optional[torch.Tensor] = None,
+                             draft_len: Optional[torch.Tensor] = None,
+                             blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
+                             kv_capacity: int = 0, stream=None) -> None:
     """Marshals one spec_verify_chain_static call: the same as
     spec_verify_chain, but the library's fixed device array is the scratch,
     for callers that cannot allocate device memory."""
@@ -256,5 +268,7 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                       fallback_eps=float(fallback_eps), n_acc=_ptr(n_acc),
                       out_tokens=_ptr(out_tokens), n_out=_ptr(n_out),
                       accept_prob=_ptr(accept_prob), residual_mass=_ptr(residual_mass),
-                      flags=_ptr(flags))
+                      flags=_ptr(flags), committed_len=_ptr(committed_len),
+                      draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
+                      block_size=int(block_size), kv_capacity=int(kv_capacity))
     _check("spec_verify_chain_static", lib().spec_verify_chain_static(ctypes.byref(a), _stream(stream)))

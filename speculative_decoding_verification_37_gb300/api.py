@@ -53,9 +53,17 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                  uniforms: Optional[torch.Tensor] = None, top_k: int = 0,
                  fallback_eps: float = 1e-6, accept_prob: bool = True,
                  residual_mass: bool = False, ws: Optional[torch.Tensor] = None,
-                 stream=None) -> ChainOut:
+                 committed_len: Optional[torch.Tensor] = None,
+                 draft_len: Optional[torch.Tensor] = None,
+                 blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
+                 kv_capacity: int = 0, stream=None) -> ChainOut:
     """target [B*(gamma+1), V], draft [B*gamma, V] (bf16 or f32, rows may be
-    strided), draft_tokens int32 [B, gamma], uniforms f32 [B, gamma+1]."""
+    strided), draft_tokens int32 [B, gamma], uniforms f32 [B, gamma+1].
+
+    With committed_len (int32 [B], on the device) the call also commits the
+    in-place K/V of the candidates: committed_len advances by n_out,
+    draft_len (if given) is cut back to it and blocks_in_use (if given)
+    follows, all on the device."""
     dev = target.device
     V = target.shape[-1]
     B = target.shape[0] // (gamma + 1)
@@ -76,7 +84,10 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                         out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws, gamma=gamma,
                         temperature=temperature, draft_logits=draft, uniforms=uniforms,
                         top_k=top_k, fallback_eps=fallback_eps, accept_prob=out.accept_prob,
-                        residual_mass=out.residual_mass, flags=out.flags, stream=stream)
+                        residual_mass=out.residual_mass, flags=out.flags,
+                        committed_len=committed_len, draft_len=draft_len,
+                        blocks_in_use=blocks_in_use, block_size=block_size,
+                        kv_capacity=kv_capacity, stream=stream)
     return out
 
 

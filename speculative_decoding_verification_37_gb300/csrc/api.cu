@@ -214,6 +214,10 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     const size_t es = esize(a->dtype);
     if (!aligned(a->target_logits, es) || (a->draft_logits && !aligned(a->draft_logits, es)))
         return SPEC_ERR_INVALID_ARG;
+    if (a->blocks_in_use && (!a->committed_len || a->block_size < 1)) return SPEC_ERR_INVALID_ARG;
+    if (a->draft_len && !a->committed_len) return SPEC_ERR_INVALID_ARG;
+    if (a->kv_capacity < 0) return SPEC_ERR_INVALID_ARG;
+    InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
     const int64_t rows = (int64_t)a->B * (a->gamma + 1);
     if (!workspace || !aligned(workspace, 256) ||
         ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
@@ -246,6 +250,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.out_tokens = a->out_tokens;
         p.n_out = a->n_out;
         p.flags = a->flags;
+        p.ip = ip;
         if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
         e = launch_argmax_verify(p, a->dtype, (int)rows, sm_count(), s);
     } else {
@@ -291,6 +296,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.amb = w.amb;
         p.qitem = w.qitem;
         p.qcap = (unsigned)(3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32));
+        p.ip = ip;
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
         // full vocabulary: the persistent kernel when the workspace, the
         // rows' alignment and the sizes allow it

@@ -247,6 +247,33 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
     return (int)(~(uint32_t)(k & 0xffffffffull));
 }
 
+// In-place KV commit of a chain request (one thread): the candidates' K/V
+// were written at cache positions len .. len+gamma before the verify, so the
+// commit advances the length by n_out (the last emitted token and the
+// accepted drafts), the draft cache's length is cut back to the same
+// boundary (never raised: with every draft accepted it has not seen the last
+// one yet) and the blocks in use follow.  A request that fails the check
+// keeps every length.
+template <typename IP>
+__device__ __forceinline__ int inplace_len0(const IP &ip, int b) {
+    return ip.len ? ip.len[b] : 0;
+}
+template <typename IP>
+__device__ __forceinline__ unsigned inplace_bad(const IP &ip, int len0, int gamma) {
+    if (!ip.len) return 0u;
+    const int64_t end = (int64_t)len0 + gamma + 1;
+    return (len0 < 0 || end > 0x7fffffffLL || (ip.capacity > 0 && end > ip.capacity)) ? SPEC_FLAG_BAD_INPUT
+                                                                                        : 0u;
+}
+template <typename IP>
+__device__ __forceinline__ void inplace_commit(const IP &ip, int b, int len0, int n_out) {
+    if (!ip.len) return;
+    const int nl = len0 + n_out;
+    ip.len[b] = nl;
+    if (ip.draft_len) ip.draft_len[b] = min(ip.draft_len[b], nl);
+    if (ip.blocks_in_use) ip.blocks_in_use[b] = (int)(((int64_t)nl + ip.block_size - 1) / ip.block_size);
+}
+
 // Sets a kernel's dynamic shared-memory limit once per device (the setting
 // is per device; doing it once keeps it out of captured launch sequences).
 template <typename K>

@@ -22,6 +22,14 @@ struct PosRec {      // one chain position's outcome, written by its cluster
 };
 constexpr unsigned REC_ACCEPT = 1u, REC_BAD_INPUT = 2u, REC_BAD_ROW = 4u, REC_FALLBACK = 8u;
 
+// In-place KV commit of a chain request: the length pointer advance done in
+// the verify call's request epilogue.
+struct InPlace {
+    int *len, *draft_len, *blocks_in_use;
+    int block_size;
+    int64_t capacity;  // 0 = unchecked
+};
+
 struct ArgmaxParams {
     const void *rows;
     int64_t stride;
@@ -41,6 +49,7 @@ struct ArgmaxParams {
     // outputs shared by both
     int *n_acc, *out_tokens, *n_out;
     unsigned *flags;
+    InPlace ip;  // chain only
 };
 
 constexpr int kTopKFastMax = 128;  // top_k served by the candidate-list path
@@ -93,6 +102,7 @@ struct SampleParams {
     int *amb;                    // [B][c][kFullAmb]
     unsigned long long *qitem;   // [qcap] queue slots
     unsigned qcap;               // 3*B*(slices the workspace was sized for)
+    InPlace ip;
 };
 
 constexpr int kTopKSlicePool = 256;  // candidates one slice of one row may hand on

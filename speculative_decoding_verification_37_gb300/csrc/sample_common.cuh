@@ -308,7 +308,8 @@ static __device__ void write_request_warp(const SampleParams &p, int b) {
     const int g = p.gamma, lane = threadIdx.x & 31;
     __threadfence();
     const PosRec *R = p.recs + (int64_t)b * (g + 1);
-    unsigned badbits = 0;
+    const int len0 = lane == 0 ? inplace_len0(p.ip, b) : 0;
+    unsigned badbits = lane == 0 ? inplace_bad(p.ip, len0, g) : 0u;
     int n = g;  // the first rejecting position (g: all accepted)
     PosRec mine{};
     for (int q0 = 0; q0 <= g; q0 += 32) {
@@ -349,6 +350,7 @@ static __device__ void write_request_warp(const SampleParams &p, int b) {
         if (lane == 0) {
             p.n_acc[b] = n;
             p.n_out[b] = n + 1;
+            inplace_commit(p.ip, b, len0, n + 1);
         }
     }
     if (lane == 0) {

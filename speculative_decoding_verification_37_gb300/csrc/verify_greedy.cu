@@ -31,9 +31,10 @@ __device__ void greedy_chain_decide(const ArgmaxParams &p, int b) {
     const int g = p.gamma, V = p.V, lane = threadIdx.x & 31;
     unsigned long long *keys = p.keys + (int64_t)b * (g + 1);
     const int *d = p.tokens + (int64_t)b * g;
-    bool bad = false;
     int n = g;  // the first mismatch (g: every draft matches)
     const int d0 = lane < g ? d[lane] : 0;  // loaded before the keys are ready
+    const int len0 = lane == 0 ? inplace_len0(p.ip, b) : 0;
+    bool bad = lane == 0 && inplace_bad(p.ip, len0, g);
     pdl_wait_primary();
     for (int k0 = 0; k0 < g; k0 += 32) {
         const int k = k0 + lane;
@@ -62,6 +63,7 @@ __device__ void greedy_chain_decide(const ArgmaxParams &p, int b) {
             p.n_acc[b] = n;
             p.n_out[b] = n + 1;
             if (p.flags) p.flags[b] = 0;
+            inplace_commit(p.ip, b, len0, n + 1);
         }
     }
     __syncwarp();

@@ -52,6 +52,7 @@ def test_struct_layouts_match_c(lib):
         printf("SpecChainArgs %zu\nSpecTreeArgs %zu\nSpecCommitArgs %zu\n",
                sizeof(SpecChainArgs), sizeof(SpecTreeArgs), sizeof(SpecCommitArgs));
         P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
+        P(SpecChainArgs, committed_len) P(SpecChainArgs, block_size) P(SpecChainArgs, kv_capacity)
         P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
         P(SpecCommitArgs, flags) P(SpecCommitArgs, num_blocks) P(SpecCommitArgs, slots_stride)
         return 0;
@@ -101,6 +102,9 @@ def _chain_args(**over):
     dict(target_logits=None), dict(target_row_stride=15), dict(n_acc=None),
     dict(draft_tokens=None), dict(uniforms=None), dict(draft_logits=None),
     dict(draft_row_stride=3), dict(target_logits=4097),
+    dict(blocks_in_use=4096),                                   # needs committed_len
+    dict(committed_len=4096, blocks_in_use=4352, block_size=0),  # needs block_size >= 1
+    dict(draft_len=4096), dict(committed_len=4096, kv_capacity=-1),
 ])
 def test_chain_host_validation(lib, bad):
     a = _chain_args(**bad)

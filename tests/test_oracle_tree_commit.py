@@ -221,3 +221,64 @@ def test_commit_rejects_bad_indices_without_writing():
                               batch.max_blocks * 4 - 2, 4)
     assert fl == O.FLAG_BAD_INPUT
     np.testing.assert_array_equal(cache, before)
+
+
+# --- in-place chain commit -----------------------------------------------------------
+def _write_in_place(cache, temp_req, table, start, n, bs):
+    """The target forward's own K/V writes: candidate i at position start+i."""
+    for i in range(n):
+        pos = start + i
+        cache[:, :, table[pos // bs], pos % bs] = temp_req[:, :, i]
+
+
+def _visible(cache, table, length, bs):
+    return np.stack([cache[:, :, table[p // bs], p % bs] for p in range(length)], axis=2) \
+        if length else np.zeros(0)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_in_place_commit_equals_the_copy_commit(seed):
+    """Writing every candidate's K/V in place and advancing the length by
+    n_out leaves the same visible cache as copying the accepted slots after
+    the verify: the rejected candidates lie past the boundary."""
+    rng = np.random.default_rng(100 + seed)
+    B, bs = 4, 4
+    gamma = int(rng.integers(0, 6))
+    S = gamma + 1
+    prefix = rng.integers(0, 21, B)
+    n_acc = rng.integers(0, gamma + 1, B)
+    batch, cache_copy, temp = _commit_case(seed, prefix, n_acc, S=S, bs=bs)
+    cache_inpl = cache_copy.copy()
+    for b in range(B):
+        table = batch.block_table[b]
+        len0 = int(prefix[b])
+        slots = O.chain_commit_slots(int(n_acc[b]))
+        new_copy, fl = O.commit_kv(cache_copy, temp[b], table, slots, len(slots), len0, bs)
+        assert fl == 0
+        _write_in_place(cache_inpl, temp[b], table, len0, S, bs)
+        c = O.commit_in_place(len0, int(n_acc[b]) + 1, gamma, bs, draft_len=len0 + gamma)
+        assert c.flags == 0 and c.committed_len == new_copy
+        np.testing.assert_array_equal(_visible(cache_inpl, table, c.committed_len, bs),
+                                      _visible(cache_copy, table, new_copy, bs))
+        # the blocks in use cover the last kept position and nothing past its block
+        assert c.blocks_in_use == (new_copy - 1) // bs + 1
+        # the draft cache (fed the last emitted token and the first gamma-1
+        # drafts) is cut back to the boundary, or keeps its gamma positions
+        assert c.draft_len == len0 + min(int(n_acc[b]) + 1, gamma)
+
+
+def test_in_place_commit_special_cases():
+    # every draft accepted: gamma+1 kept, the draft cache keeps what it has
+    c = O.commit_in_place(10, 5, 4, 16, draft_len=14)
+    assert (c.committed_len, c.draft_len, c.blocks_in_use, c.flags) == (15, 14, 1, 0)
+    # a rejection at the first draft: only the last emitted token is kept
+    c = O.commit_in_place(16, 1, 4, 16, draft_len=20)
+    assert (c.committed_len, c.draft_len, c.blocks_in_use) == (17, 17, 2)
+    # gamma 0: the bonus round keeps one position
+    assert O.commit_in_place(0, 1, 0, 8).committed_len == 1
+    # reserved positions past the capacity, or a negative length: nothing moves
+    for len0, cap in ((60, 64), (-1, 0)):
+        c = O.commit_in_place(len0, 1, 4, 16, draft_len=7, kv_capacity=cap)
+        assert (c.committed_len, c.draft_len, c.blocks_in_use, c.flags) == (len0, 7, None, O.FLAG_BAD_INPUT)
+    assert O.commit_in_place(59, 5, 4, 16, kv_capacity=64).flags == 0      # ends exactly at 64
+    assert O.commit_in_place(2**31 - 5, 1, 4, 16).flags == O.FLAG_BAD_INPUT
