@@ -560,6 +560,146 @@ def run_ngram(args, rank, world, local):
                           "kernel_source": kernel_source_hash()}), flush=True)
 
 
+TREE_BUILD_METRIC = "draft trees built level by level: trees/s + draft-logit GB/s vs peak"
+
+
+def tree_build_oracle_sample(levels, spec, seconds: float):
+    """Times the oracle's tree build on this host, one request at a time over
+    the batch's first requests, for about `seconds`."""
+    import oracle as O
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds and n < spec.B:
+        rows = [lv[n * h:(n + 1) * h].double().numpy() for lv, h in zip(levels, spec.topHead)]
+        O.build_tree(rows, spec.topKSpec, spec.topHead)
+        n += 1
+    el = time.perf_counter() - t0
+    return n / el, (f"{n} trees of the batch ({spec.n_rows} draft rows of {spec.V} logits each), "
+                    f"{el:.1f} s on one core")
+
+
+def run_tree_build(args, rank, world, local):
+    """The draft-tree builder over the tree workload's shape: one step is the
+    three level calls of a whole tree (captured in one CUDA graph), the draft
+    rows resident; L2 flushed between steps."""
+    import dataclasses
+    spec = W.CONFIGS[4] if not args.batch else dataclasses.replace(W.CONFIGS[4], B=args.batch)
+    levels = W.make_tree_levels(spec, seed=rank)
+    logit_bytes = sum(lv.numel() * lv.element_size() for lv in levels)
+    cfg = {"workload": f"tree build {[list(k) for k in spec.topKSpec]}/{list(spec.topHead)} "
+                       f"B={spec.B} V={spec.V} {spec.dtype}",
+           "B_per_gpu": spec.B, "V": spec.V, "dtype": spec.dtype,
+           "topKSpec": [list(k) for k in spec.topKSpec], "topHead": list(spec.topHead),
+           "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+           "parallelism": f"dp{world} (independent request shards, no collective)"}
+    if args.impl == "reference":
+        if rank == 0:
+            v, sample = tree_build_oracle_sample(levels, spec, seconds=max(2.0, 2.0 * args.steps))
+            print(json.dumps({"impl": "reference", "metric": TREE_BUILD_METRIC, "value": v, "unit": "trees/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                              "dtype": spec.dtype, "data": "synthetic", "config": cfg,
+                              "cpu_baseline": {"value": v, "unit": "trees/s", "cores": 1, "kind": "oracle",
+                                               "sample": sample},
+                              "e2e": {"value": v, "unit": "trees/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    from speculative_decoding_verification_37_gb300 import build as _b
+    from speculative_decoding_verification_37_gb300 import api
+    _b.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d_levels = [lv.to(dev) for lv in levels]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tb = api.TreeBuilder(spec.B, spec.V, spec.topKSpec, spec.topHead, dev)
+
+    def build_all():
+        for i, lv in enumerate(d_levels):
+            tb.level(lv, i)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            build_all()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        build_all()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    # per-level launch times (eager, events between the calls)
+    lvl_ms = [[] for _ in d_levels]
+    for _ in range(3):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(d_levels) + 1)]
+        ev[0].record()
+        for i, lv in enumerate(d_levels):
+            tb.level(lv, i)
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        for i in range(len(d_levels)):
+            lvl_ms[i].append(ev[i].elapsed_time(ev[i + 1]))
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier(world)
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    barrier(world)
+    clk = clocks.stop()
+    t = max_over_ranks(statistics.mean(times), world)
+    peak, peak_kind = measured_peaks()
+    achieved = logit_bytes / (t * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        h_levels = [lv.pin_memory() for lv in levels]
+        et = []
+        for i in range(5):
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for d, h in zip(d_levels, h_levels):
+                d.copy_(h, non_blocking=True)
+            build_all()
+            host = [x.to("cpu", non_blocking=True) for x in (tb.node_token, tb.node_parent, tb.row_of_node)]
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                et.append(e0.elapsed_time(e1))
+        te = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": spec.B * world / (te * 1e-3), "unit": "trees/s", "h2d_bytes_per_step": logit_bytes,
+               "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+               "ms_per_step": round(te, 4)}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample = tree_build_oracle_sample(levels, spec, seconds=8.0)
+        cpu = {"value": v, "unit": "trees/s", "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({"metric": TREE_BUILD_METRIC, "value": spec.B * world / (t * 1e-3), "unit": "trees/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 5),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+                          "data": "synthetic", "config": cfg,
+                          "roofline": {"bound": "hbm", "kernel": "tree_level_kernel", "achieved": round(achieved, 1),
+                                       "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                                       "traffic": None, "algorithmic_bytes": logit_bytes,
+                                       "avg_launch_ms": round(t / len(d_levels), 5),
+                                       "level_ms": [round(statistics.mean(x), 5) for x in lvl_ms],
+                                       "level_bytes": [lv.numel() * lv.element_size() for lv in levels],
+                                       "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+                          "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * len(d_levels),
+                          "clocks": clk, "kernel_source": kernel_source_hash()}), flush=True)
+
+
 def ngram_oracle_sample(hist, lens, spec, seconds: float):
     """Times the oracle on this host, one request at a time over the batch's
     first requests, for about `seconds`."""
@@ -584,8 +724,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's request count (smaller cases for profiling)")
-    ap.add_argument("--workload", default="verify", choices=["verify", "ngram"],
-                    help="ngram: the prompt-lookup drafter on long token histories instead")
+    ap.add_argument("--workload", default="verify", choices=["verify", "ngram", "tree_build"],
+                    help="ngram: the prompt-lookup drafter on long token histories; tree_build: "
+                         "the draft-tree builder on the tree workload's shape")
     ap.add_argument("--kv-commit", default="copy", choices=["copy", "inplace"],
                     help="inplace (chain): K/V written in place by the forward, the verify "
                          "call advances the lengths, no commit kernel")
@@ -593,6 +734,9 @@ def main():
     rank, world, local = dist_setup()
     if args.workload == "ngram":
         run_ngram(args, rank, world, local)
+        return
+    if args.workload == "tree_build":
+        run_tree_build(args, rank, world, local)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -81,6 +81,8 @@ extern "C" {
 #define SPEC_WS_CHAIN_FULL 4 /* n = gamma: SPEC_WS_CHAIN plus the per-slice statistics, draw
                                 state and work queue of the persistent full-vocabulary path
                                 (top_k == 0; about 2 KiB per request position at V = 128,256) */
+#define SPEC_WS_TREE_LEVEL 5 /* n = H (parents a spec_tree_level call expands): one 144-byte
+                                summary per (row, 2048-logit slice) and per row */
 
 /*
  * Chain verification, sampled (temperature > 0) or greedy (temperature == 0).
@@ -343,6 +345,66 @@ typedef struct SpecNgramArgs {
 } SpecNgramArgs;
 
 int spec_ngram_draft(const SpecNgramArgs *args, void *stream);
+
+/*
+ * One level of a draft tree ("投机推理：小模型搭树，大模型一次验证",
+ * 树形投机怎么配置 and its three expansion steps; the real dump example).  The
+ * draft model has run once at each of this level's H parents; for every
+ * request b this call
+ *   - gives parent j (row b*H + j of `logits`) the k[j] tokens with the
+ *     largest logits as children (ties to the lower token id), numbered
+ *     n_before+1, n_before+2, ... in parent order, then rank order;
+ *   - sets each child's path log-probability to its parent's plus the draft's
+ *     log-softmax (temperature 1) at its token;
+ *   - picks the n_next children with the highest path log-probability (ties
+ *     to the lower node id) as the next level's parents, written in id order
+ *     to next_parents[b], and gives them logits rows next_row0, next_row0+1,
+ *     ... in row_of_node (every other new node gets -1).
+ * The root's level passes parents = NULL and H = 1; it also writes node 0's
+ * log-probability (0) and row (0).  A full tree is built by calling this once
+ * per level with that level's draft rows, passing the previous call's
+ * next_parents as `parents`.
+ *
+ * Layout: node_token/node_parent [B][N] hold node id i at index i-1;
+ *   node_logp/row_of_node [B][N+1] are indexed by node id (the root is 0).
+ *   These are in/out: the call reads the parents' log-probabilities and
+ *   writes only the new nodes' entries (and the chosen nodes' rows).
+ * Limits: 1 <= H <= 64, 1 <= k[j] <= min(16, V), sum(k) <= 256,
+ *   0 <= n_next <= min(64, sum(k)), n_before + sum(k) <= N.
+ * Errors: SPEC_ERR_INVALID_ARG for arguments outside those limits, a NULL
+ *   required pointer, a misaligned row or a short workspace (nothing is
+ *   launched).  A parent id outside [0, n_before] flags SPEC_FLAG_BAD_INPUT,
+ *   a row holding a NaN or with no finite maximum SPEC_FLAG_BAD_ROW; such a
+ *   request writes no nodes, its next_parents are -1 (so the next level
+ *   flags it too) and its flags[b] gets the bit.
+ * Workspace: spec_workspace_bytes(SPEC_WS_TREE_LEVEL, B, H, V) bytes (no
+ *   zeroing needed; calls sharing it must be ordered on one stream).
+ *   Asynchronous on `stream` (two launches, the second a programmatic
+ *   dependent of the first).
+ */
+#define SPEC_TREE_MAX_HEADS 64
+#define SPEC_TREE_MAX_K 16
+#define SPEC_TREE_MAX_LEVEL_NODES 256
+typedef struct SpecTreeLevelArgs {
+    int32_t B, V, dtype;
+    int32_t H;                          /* parents expanded at this level */
+    int32_t k[SPEC_TREE_MAX_HEADS];     /* k[j]: children of parent j (j < H) */
+    int32_t n_next;                     /* parents the next level expands (0: last level) */
+    int32_t N;                          /* nodes the per-request arrays hold */
+    int32_t n_before;                   /* nodes already in the tree */
+    int32_t next_row0;                  /* logits rows given out so far, this level's included */
+    const void *logits;                 /* device [B*H rows][V], bf16 or f32 */
+    int64_t row_stride;                 /* elements between rows (>= V) */
+    const int32_t *parents;             /* device [B][H], ascending node ids; NULL at the root */
+    int32_t *node_token;                /* device in/out [B][N] */
+    int32_t *node_parent;               /* device in/out [B][N] */
+    float *node_logp;                   /* device in/out [B][N+1] */
+    int32_t *row_of_node;               /* device in/out [B][N+1] */
+    int32_t *next_parents;              /* device out [B][n_next] (may be NULL if n_next == 0) */
+    uint32_t *flags;                    /* device in/out [B] (bits OR'ed in) or NULL */
+} SpecTreeLevelArgs;
+
+int spec_tree_level(const SpecTreeLevelArgs *args, void *workspace, size_t ws_bytes, void *stream);
 
 /* Diagnostic: the largest relative error of the GPU's hardware exponential
  * (ex2.approx.ftz.f32) against fp64 over every fp32 input in [-126, 1], on the

@@ -34,8 +34,10 @@ import numpy as np
 
 FLAG_BAD_INPUT = 1
 FLAG_BAD_ROW = 4
-SELECT_MARGIN = 1e-5   # a selection whose last kept and first dropped path
-                       # log-probabilities are closer than this is a boundary case
+SELECT_MARGIN = 5e-5   # a selection whose last kept and first dropped path
+                       # log-probabilities are closer than this (but not tied
+                       # siblings, which compare equal in any precision) is a
+                       # boundary case
 
 
 @dataclass
@@ -89,8 +91,10 @@ def expand_level(rows: np.ndarray, parents: Sequence[int], parent_logp: Sequence
     chosen = ranked[:n_next]
     out.next_parents = sorted(ids[i] for i in chosen)
     if 0 < n_next < n:
-        gap = out.node_logp[ranked[n_next - 1]] - out.node_logp[ranked[n_next]]
-        out.boundary = gap < SELECT_MARGIN
+        a, b = ranked[n_next - 1], ranked[n_next]
+        gap = out.node_logp[a] - out.node_logp[b]
+        siblings_tied = gap == 0 and out.node_parent[a] == out.node_parent[b]
+        out.boundary = bool(gap < SELECT_MARGIN) and not siblings_tied
     return out
 
 

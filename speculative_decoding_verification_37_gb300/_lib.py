@@ -21,11 +21,13 @@ SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
 SPEC_DTYPE_BF16, SPEC_DTYPE_F32 = 0, 1
 SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW, SPEC_FLAG_TIMEOUT = 1, 2, 4, 8
 SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT, SPEC_WS_CHAIN_TOPK, SPEC_WS_CHAIN_FULL = 0, 1, 2, 3, 4
+SPEC_WS_TREE_LEVEL = 5
+SPEC_TREE_MAX_HEADS = 64
 TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspace holds it
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
             "spec_get_status", "spec_error_string", "spec_last_cuda_error",
-            "spec_verify_chain_static", "spec_selftest_ex2", "spec_ngram_draft")
+            "spec_verify_chain_static", "spec_selftest_ex2", "spec_ngram_draft", "spec_tree_level")
 
 
 class SpecChainArgs(ctypes.Structure):
@@ -67,6 +69,15 @@ class SpecNgramArgs(ctypes.Structure):
                 ("match_start", c_void_p), ("flags", c_void_p)]
 
 
+class SpecTreeLevelArgs(ctypes.Structure):
+    _fields_ = [("B", c_int32), ("V", c_int32), ("dtype", c_int32), ("H", c_int32),
+                ("k", c_int32 * SPEC_TREE_MAX_HEADS), ("n_next", c_int32), ("N", c_int32),
+                ("n_before", c_int32), ("next_row0", c_int32), ("logits", c_void_p),
+                ("row_stride", c_int64), ("parents", c_void_p), ("node_token", c_void_p),
+                ("node_parent", c_void_p), ("node_logp", c_void_p), ("row_of_node", c_void_p),
+                ("next_parents", c_void_p), ("flags", c_void_p)]
+
+
 class SpecError(RuntimeError):
     def __init__(self, fn: str, code: int):
         msg = f"{fn} returned {code} ({lib().spec_error_string(code).decode()})"
@@ -106,6 +117,8 @@ def lib():
         L.spec_selftest_ex2.restype = c_int
         L.spec_ngram_draft.argtypes = [POINTER(SpecNgramArgs), c_void_p]
         L.spec_ngram_draft.restype = c_int
+        L.spec_tree_level.argtypes = [POINTER(SpecTreeLevelArgs), c_void_p, c_size_t, c_void_p]
+        L.spec_tree_level.restype = c_int
         _LIB = L
     return _LIB
 
@@ -154,6 +167,27 @@ def spec_ngram_draft(*, history: torch.Tensor, hist_len: torch.Tensor, gamma: in
                       draft_tokens=_ptr(draft_tokens), n_draft=_ptr(n_draft), match_n=_ptr(match_n),
                       match_start=_ptr(match_start), flags=_ptr(flags))
     _check("spec_ngram_draft", lib().spec_ngram_draft(ctypes.byref(a), _stream(stream)))
+
+
+def spec_tree_level(*, logits: torch.Tensor, H: int, k, n_next: int, n_before: int, next_row0: int,
+                    node_token: torch.Tensor, node_parent: torch.Tensor, node_logp: torch.Tensor,
+                    row_of_node: torch.Tensor, workspace: torch.Tensor,
+                    parents: Optional[torch.Tensor] = None, next_parents: Optional[torch.Tensor] = None,
+                    flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Marshals one spec_tree_level call: logits [B*H, V] (row stride =
+    stride(0)), node arrays [B, N] / [B, N+1], parents [B, H] or None at the
+    root, next_parents [B, n_next]."""
+    B = logits.shape[0] // H
+    kk = (c_int32 * SPEC_TREE_MAX_HEADS)(*[int(x) for x in k])
+    a = SpecTreeLevelArgs(B=B, V=logits.shape[-1], dtype=_dtype_code(logits), H=H, k=kk,
+                          n_next=n_next, N=node_token.shape[-1], n_before=n_before,
+                          next_row0=next_row0, logits=_ptr(logits), row_stride=logits.stride(0),
+                          parents=_ptr(parents), node_token=_ptr(node_token),
+                          node_parent=_ptr(node_parent), node_logp=_ptr(node_logp),
+                          row_of_node=_ptr(row_of_node), next_parents=_ptr(next_parents),
+                          flags=_ptr(flags))
+    _check("spec_tree_level", lib().spec_tree_level(ctypes.byref(a), _ptr(workspace),
+                                                    workspace.numel(), _stream(stream)))
 
 
 def spec_selftest_ex2() -> float:

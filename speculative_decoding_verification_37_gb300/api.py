@@ -165,3 +165,48 @@ def ngram_draft(history: torch.Tensor, hist_len: torch.Tensor, *, gamma: int, n_
                        draft_tokens=out.draft_tokens, n_draft=out.n_draft, match_n=out.match_n,
                        match_start=out.match_start, flags=out.flags, stream=stream)
     return out
+
+
+class TreeBuilder:
+    """Builds draft trees for B requests one level at a time on the device
+    (topKSpec / topHead shape).  Between levels the caller runs the draft
+    model at ``next_parents`` and passes its logits rows, in that order, to
+    the next ``level`` call.  Node arrays follow the tree verify's layout:
+    node_token / node_parent [B, N] (node id i at index i-1), node_logp /
+    row_of_node [B, N+1] (indexed by node id, the root is 0)."""
+
+    def __init__(self, B: int, V: int, topKSpec, topHead, device, flags: bool = True):
+        if len(topKSpec) != len(topHead) or not len(topHead) or topHead[0] != 1:
+            raise ValueError("topHead must start with 1 (the root) and match topKSpec")
+        self.B, self.V = B, V
+        self.topKSpec = [list(map(int, ks)) for ks in topKSpec]
+        self.topHead = list(map(int, topHead))
+        self.N = sum(sum(ks) for ks in self.topKSpec)
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.node_token = torch.full((B, self.N), -1, **i32)
+        self.node_parent = torch.full((B, self.N), -1, **i32)
+        self.node_logp = torch.zeros((B, self.N + 1), dtype=torch.float32, device=dev)
+        self.row_of_node = torch.full((B, self.N + 1), -1, **i32)
+        self.flags = torch.zeros(B, **i32) if flags else None
+        self.next = [torch.empty((B, h), **i32) for h in self.topHead[1:]] + [None]
+        self.ws = [workspace(L.SPEC_WS_TREE_LEVEL, B, h, V, dev) for h in self.topHead]
+        self.level_index = 0
+
+    def level(self, logits: torch.Tensor, i: Optional[int] = None, stream=None) -> Optional[torch.Tensor]:
+        """Expand level i (default: the next one) from its draft rows
+        [B*topHead[i], V]; returns the next level's parents [B, topHead[i+1]]
+        (None after the last level)."""
+        i = self.level_index if i is None else i
+        H = self.topHead[i]
+        n_before = sum(sum(ks) for ks in self.topKSpec[:i])
+        next_row0 = sum(self.topHead[:i + 1])
+        n_next = self.topHead[i + 1] if i + 1 < len(self.topHead) else 0
+        L.spec_tree_level(logits=logits, H=H, k=self.topKSpec[i], n_next=n_next, n_before=n_before,
+                          next_row0=next_row0, node_token=self.node_token,
+                          node_parent=self.node_parent, node_logp=self.node_logp,
+                          row_of_node=self.row_of_node, workspace=self.ws[i],
+                          parents=None if i == 0 else self.next[i - 1],
+                          next_parents=self.next[i], flags=self.flags, stream=stream)
+        self.level_index = i + 1
+        return self.next[i]

@@ -175,6 +175,29 @@ const DdExpTables &exp_tables() {
 
 }  // namespace
 
+namespace {
+
+// Tree-level workspace: header (status) | slice summaries [B*H*slices] |
+// row results [B*H].
+size_t tree_level_layout(int32_t B, int32_t H, int32_t V, void *base, TreeLevelParams *p) {
+    const size_t rows = (size_t)B * (size_t)H;
+    const size_t slices = ((size_t)V + kTlSliceElems - 1) / kTlSliceElems;
+    size_t off = kWsHeader;
+    const size_t o_it = off;
+    off += ws_align(rows * slices * sizeof(TlItem));
+    const size_t o_rr = off;
+    off += ws_align(rows * sizeof(TlRow));
+    if (p) {
+        char *c = static_cast<char *>(base);
+        p->status = reinterpret_cast<unsigned *>(c);
+        p->items = reinterpret_cast<TlItem *>(c + o_it);
+        p->rowrec = reinterpret_cast<TlRow *>(c + o_rr);
+    }
+    return off;
+}
+
+}  // namespace
+
 extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V) {
     if (B < 0 || n < 0 || V < 0) return 0;
     switch (kind) {
@@ -189,6 +212,8 @@ extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V
         return ws_layout_bytes(B, 0, (size_t)B * (size_t)n * sizeof(unsigned long long), nullptr, nullptr);
     case SPEC_WS_COMMIT:
         return kWsHeader + ws_align((size_t)B * sizeof(unsigned));
+    case SPEC_WS_TREE_LEVEL:
+        return tree_level_layout(B, n, V, nullptr, nullptr);
     default:
         return 0;
     }
@@ -426,6 +451,60 @@ extern "C" int spec_commit_kv(const SpecCommitArgs *a, void *workspace, size_t w
     // one block per (request, slot, group); blocks past n_slots exit at once
     if ((int64_t)a->B * a->S * p.groups > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
     const cudaError_t e = launch_commit_kv(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
+extern "C" int spec_tree_level(const SpecTreeLevelArgs *a, void *workspace, size_t ws_bytes, void *stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->B < 0 || a->V < 1 || a->H < 1 || a->H > kTreeMaxHeads) return SPEC_ERR_INVALID_ARG;
+    if (a->dtype != SPEC_DTYPE_BF16 && a->dtype != SPEC_DTYPE_F32) return SPEC_ERR_INVALID_ARG;
+    TreeLevelParams p = {};
+    int kmax = 0;
+    p.koff[0] = 0;
+    for (int j = 0; j < a->H; ++j) {
+        const int k = a->k[j];
+        if (k < 1 || k > kTreeMaxK || k > a->V) return SPEC_ERR_INVALID_ARG;
+        kmax = k > kmax ? k : kmax;
+        p.koff[j + 1] = p.koff[j] + k;
+        if (p.koff[j + 1] > kTreeMaxLevelNodes) return SPEC_ERR_INVALID_ARG;
+        for (int i = p.koff[j]; i < p.koff[j + 1]; ++i) p.head_of[i] = (unsigned char)j;
+    }
+    const int n = p.koff[a->H];
+    if (a->n_next < 0 || a->n_next > 64 || a->n_next > n) return SPEC_ERR_INVALID_ARG;
+    if (a->n_before < 0 || a->N < 1 || (int64_t)a->n_before + n > a->N) return SPEC_ERR_INVALID_ARG;
+    if (a->next_row0 < 1 || (int64_t)a->next_row0 + a->n_next > 0x7fffffffLL) return SPEC_ERR_INVALID_ARG;
+    if (!a->parents && (a->H != 1 || a->n_before != 0)) return SPEC_ERR_INVALID_ARG;
+    if (a->B == 0) return SPEC_OK;
+    const size_t es = esize(a->dtype);
+    if (!a->logits || !aligned(a->logits, es) || a->row_stride < a->V) return SPEC_ERR_INVALID_ARG;
+    if (!a->node_token || !a->node_parent || !a->node_logp || !a->row_of_node) return SPEC_ERR_INVALID_ARG;
+    if (a->n_next > 0 && !a->next_parents) return SPEC_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)a->B * a->H;
+    const int64_t slices = ((int64_t)a->V + kTlSliceElems - 1) / kTlSliceElems;
+    if (rows * slices > 0x7fffffffLL || (int64_t)a->B * (a->N + 1) > (int64_t)1 << 40) return SPEC_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < spec_workspace_bytes(SPEC_WS_TREE_LEVEL, a->B, a->H, a->V))
+        return SPEC_ERR_INVALID_ARG;
+    tree_level_layout(a->B, a->H, a->V, workspace, &p);
+    p.rows = a->logits;
+    p.stride = a->row_stride;
+    p.B = a->B;
+    p.V = a->V;
+    p.H = a->H;
+    p.slices = (int)slices;
+    p.n_nodes = n;
+    p.n_next = a->n_next;
+    p.N = a->N;
+    p.n_before = a->n_before;
+    p.next_row0 = a->next_row0;
+    p.root = a->parents ? 0 : 1;
+    p.parents = a->parents;
+    p.node_token = a->node_token;
+    p.node_parent = a->node_parent;
+    p.node_logp = a->node_logp;
+    p.row_of_node = a->row_of_node;
+    p.next_parents = a->next_parents;
+    p.flags = a->flags;
+    const cudaError_t e = launch_tree_level(p, a->dtype, kmax, sm_count(), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 

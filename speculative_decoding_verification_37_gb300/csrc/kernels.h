@@ -119,6 +119,39 @@ struct CommitParams {
     unsigned *flags, *status, *counters;  // counters: one per request, zero between calls
 };
 
+// ---------------------------------------------------------------------------
+// draft-tree builder: one level (the parents' draft rows -> children, path
+// log-probabilities, next parents)
+// ---------------------------------------------------------------------------
+constexpr int kTreeMaxHeads = 64, kTreeMaxK = 16, kTreeMaxLevelNodes = 256;
+constexpr int kTlSliceElems = 2048;  // logits of a row one warp item covers
+
+struct TlItem {                    // one (row, slice) item's summary
+    unsigned long long key[kTreeMaxK];  // its K largest (value, lowest index) keys, 0 = none
+    float m, s;                    // slice max and sum of exp(x - m)
+    unsigned nan, pad;
+};
+struct TlRow {                     // one row's result
+    int tok[kTreeMaxK];            // top tokens, larger logit first
+    float lq[kTreeMaxK];           // their log-softmax values
+    unsigned bad, pad[3];
+};
+
+struct TreeLevelParams {
+    const void *rows;
+    int64_t stride;
+    int B, V, H, slices, n_nodes, n_next, N, n_before, next_row0, root;
+    int koff[kTreeMaxHeads + 1];                // prefix sums of the children counts
+    unsigned char head_of[kTreeMaxLevelNodes];  // parent slot of each new node
+    const int *parents;
+    int *node_token, *node_parent, *row_of_node, *next_parents;
+    float *node_logp;
+    unsigned *flags, *status;
+    TlItem *items;
+    TlRow *rowrec;
+};
+cudaError_t launch_tree_level(const TreeLevelParams &p, int dtype, int kmax, int sms, cudaStream_t s);
+
 cudaError_t launch_argmax_verify(const ArgmaxParams &p, int dtype, int n_rows, int sms, cudaStream_t s);
 int argmax_stage_bytes();  // a greedy slice body must fit this
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);

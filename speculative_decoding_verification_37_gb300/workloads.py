@@ -25,7 +25,7 @@ which are exact in float32 and float64 and lie in [0, 1).
 from __future__ import annotations
 
 from dataclasses import dataclass, field
-from typing import Optional, Sequence
+from typing import List, Optional, Sequence
 
 import numpy as np
 import torch
@@ -340,6 +340,28 @@ def make_tree(spec: TreeSpec, seed: int = 0, requests: Optional[Sequence[int]] =
         toks[i], pars[i], rows[i] = tree.node_token, tree.node_parent, tree.row_of_node
     logits = _to_torch(tgt32.reshape(n * R, V), spec.dtype)
     return TreeBatch(spec, reqs, logits, toks, pars, rows)
+
+
+def make_tree_levels(spec: TreeSpec, seed: int = 0,
+                     requests: Optional[Sequence[int]] = None) -> List[torch.Tensor]:
+    """Draft logits for building the trees of ``spec`` level by level: entry
+    i is [n*topHead[i], V] in the spec's dtype, row b*topHead[i] + j being the
+    draft's logits at parent j of level i of request b.  They are the draft
+    rows ``make_tree`` grows its trees from (target rows plus draft noise,
+    same seeds), so the expanded parents' rows line up with its logits rows."""
+    reqs = np.arange(spec.B) if requests is None else np.asarray(requests, dtype=np.int64)
+    R, V, n = spec.n_rows, spec.V, len(reqs)
+    rows = np.empty((n, R, V), np.float32)
+    for i, b in enumerate(reqs):
+        x = _rng(seed, SEED_TARGET, b).standard_normal((R, V), dtype=np.float32)
+        x *= np.float32(spec.target_sigma)
+        e = _rng(seed, SEED_DRAFT_NOISE, b).standard_normal((R, V), dtype=np.float32)
+        rows[i] = x + np.float32(spec.draft_sigma) * e
+    out, r0 = [], 0
+    for h in spec.topHead:
+        out.append(_to_torch(np.ascontiguousarray(rows[:, r0:r0 + h]).reshape(n * h, V), spec.dtype))
+        r0 += h
+    return out
 
 
 # --------------------------------------------------------------------------

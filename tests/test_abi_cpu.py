@@ -49,8 +49,11 @@ def test_struct_layouts_match_c(lib):
     #include "spec_verify.h"
     #define P(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
     int main(void) {
-        printf("SpecChainArgs %zu\nSpecTreeArgs %zu\nSpecCommitArgs %zu\n",
-               sizeof(SpecChainArgs), sizeof(SpecTreeArgs), sizeof(SpecCommitArgs));
+        printf("SpecChainArgs %zu\nSpecTreeArgs %zu\nSpecCommitArgs %zu\nSpecTreeLevelArgs %zu\n",
+               sizeof(SpecChainArgs), sizeof(SpecTreeArgs), sizeof(SpecCommitArgs),
+               sizeof(SpecTreeLevelArgs));
+        P(SpecTreeLevelArgs, k) P(SpecTreeLevelArgs, logits) P(SpecTreeLevelArgs, row_stride)
+        P(SpecTreeLevelArgs, flags) P(SpecTreeLevelArgs, next_row0)
         P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
         P(SpecChainArgs, committed_len) P(SpecChainArgs, block_size) P(SpecChainArgs, kv_capacity)
         P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
@@ -66,7 +69,7 @@ def test_struct_layouts_match_c(lib):
         lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(line.split() for line in lines if line)
     structs = {"SpecChainArgs": L.SpecChainArgs, "SpecTreeArgs": L.SpecTreeArgs,
-               "SpecCommitArgs": L.SpecCommitArgs}
+               "SpecCommitArgs": L.SpecCommitArgs, "SpecTreeLevelArgs": L.SpecTreeLevelArgs}
     for name, cls in structs.items():
         assert int(got[name]) == ctypes.sizeof(cls), name
     for key, val in got.items():
@@ -154,3 +157,42 @@ def test_tree_and_commit_host_validation(lib):
 def test_error_strings(lib):
     assert lib.spec_error_string(L.SPEC_ERR_INVALID_ARG) == b"invalid argument"
     assert lib.spec_error_string(12345) == b"unknown error code"
+
+
+def _level_args(**over):
+    k = (ctypes.c_int32 * L.SPEC_TREE_MAX_HEADS)(*([2, 2] + [0] * (L.SPEC_TREE_MAX_HEADS - 2)))
+    a = L.SpecTreeLevelArgs(B=2, V=100, dtype=L.SPEC_DTYPE_F32, H=2, k=k, n_next=2, N=12, n_before=6,
+                            next_row0=3, logits=4096, row_stride=100, parents=256, node_token=512,
+                            node_parent=768, node_logp=1024, row_of_node=1280, next_parents=1536,
+                            flags=None)
+    for key, v in over.items():
+        setattr(a, key, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=0), dict(H=65), dict(V=0), dict(dtype=5), dict(n_next=-1), dict(n_next=5), dict(n_next=65),
+    dict(n_before=-1), dict(N=9), dict(next_row0=0), dict(parents=None), dict(logits=None),
+    dict(logits=4098), dict(row_stride=99), dict(node_logp=None), dict(next_parents=None),
+])
+def test_tree_level_host_validation(lib, bad):
+    a = _level_args(**bad)
+    ws = ctypes.create_string_buffer(1 << 20)
+    assert lib.spec_tree_level(ctypes.byref(a), ws, 1 << 20, None) == L.SPEC_ERR_INVALID_ARG
+
+
+def test_tree_level_children_limits(lib):
+    ws = ctypes.create_string_buffer(1 << 20)
+    for ks in ([0, 2], [17, 2], [101, 1]):
+        a = _level_args()
+        a.k[0], a.k[1] = ks
+        assert lib.spec_tree_level(ctypes.byref(a), ws, 1 << 20, None) == L.SPEC_ERR_INVALID_ARG
+    a = _level_args(H=20, N=400, n_next=0)
+    for j in range(20):
+        a.k[j] = 16                                       # 320 children > 256 per level
+    assert lib.spec_tree_level(ctypes.byref(a), ws, 1 << 20, None) == L.SPEC_ERR_INVALID_ARG
+    a = _level_args()
+    assert lib.spec_tree_level(ctypes.byref(a), None, 0, None) == L.SPEC_ERR_INVALID_ARG
+    assert lib.spec_tree_level(ctypes.byref(a), ctypes.c_void_p(4096), 64, None) == L.SPEC_ERR_INVALID_ARG
+    assert lib.spec_tree_level(ctypes.byref(_level_args(B=0)), None, 0, None) == L.SPEC_OK
+    assert L.spec_workspace_bytes(L.SPEC_WS_TREE_LEVEL, 128, 2, 128256) >= 128 * 2 * 32 * 144

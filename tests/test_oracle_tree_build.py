@@ -153,6 +153,12 @@ def test_boundary_flag_on_near_tie():
     assert lv.boundary and lv.next_parents == [1] and lv.node_token == [1, 0]
     lv = O.expand_level(np.array([[0.0, 0.5, -5.0]]), [0], [0.0], [2], 0, 1)
     assert not lv.boundary
+    # tied siblings are decided by the node id in any precision: no boundary
+    lv = O.expand_level(np.array([[0.5, 0.5, -5.0]]), [0], [0.0], [2], 0, 1)
+    assert not lv.boundary and lv.next_parents == [1] and lv.node_token == [0, 1]
+    # equal path probabilities under different parents are a boundary case
+    lv = O.expand_level(np.array([[0.5, -5.0], [0.5, -5.0]]), [1, 2], [-1.0, -1.0], [1, 1], 2, 1)
+    assert lv.boundary
 
 
 @pytest.mark.parametrize("seed", range(3))
