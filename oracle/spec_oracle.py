@@ -53,6 +53,8 @@ EPS_BAND = 0.5           # a residual mass within EPS_BAND * eps of eps is a bou
 FLAG_BAD_INPUT = 1       # a token, parent or row index out of range: request skipped
 FLAG_FALLBACK = 2        # the residual-mass fallback was used
 FLAG_BAD_ROW = 4         # a row whose kept logits are all -inf (no distribution)
+FLAG_EOS = 16            # the round's output was cut after an end-of-sequence token
+FLAG_LIMIT = 32          # the round's output was cut at the request's remaining length
 
 
 # ---------------------------------------------------------------------------
@@ -332,6 +334,38 @@ def verify_tree(logits: np.ndarray, node_token: np.ndarray, node_parent: np.ndar
     res.tokens = [tok[c - 1] for c in res.path] + ([] if extra is None else [extra])
     res.commit_slots = [0] + res.path
     return res
+
+
+# ---------------------------------------------------------------------------
+# round termination: EOS and the length limit                      [KV4 §5]
+# ---------------------------------------------------------------------------
+def truncate_round(r: ChainResult, eos: Optional[int] = None,
+                   max_new: Optional[int] = None) -> ChainResult:
+    """A round emits its accepted drafts and one drawn token, but an
+    end-of-sequence token or the request's length limit ends it early
+    ([KV4 §5]).  Reading: the emitted tokens are cut right after the first
+    `eos` (the EOS itself is emitted), then to at most `max_new` tokens (a
+    limit <= 0 emits nothing); n_acc counts the accepted drafts still
+    emitted.  FLAG_EOS / FLAG_LIMIT say which cut shortened the round (an
+    EOS that is the last token kept also sets FLAG_EOS).  A flagged (bad)
+    round is returned unchanged."""
+    if r.flags & (FLAG_BAD_INPUT | FLAG_BAD_ROW):
+        return r
+    tokens = list(r.tokens)
+    flags = r.flags
+    if eos is not None:
+        for i, t in enumerate(tokens):
+            if t == eos:
+                tokens = tokens[:i + 1]
+                flags |= FLAG_EOS
+                break
+    if max_new is not None and len(tokens) > max(max_new, 0):
+        tokens = tokens[:max(max_new, 0)]
+        flags |= FLAG_LIMIT
+        if eos is not None and eos not in tokens:
+            flags &= ~FLAG_EOS
+    return ChainResult(n_acc=min(r.n_acc, len(tokens)), tokens=tokens, accept_prob=r.accept_prob,
+                       residual_mass=r.residual_mass, flags=flags, boundary=r.boundary)
 
 
 # ---------------------------------------------------------------------------

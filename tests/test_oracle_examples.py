@@ -233,3 +233,55 @@ def test_greedy_lowest_index_tie_break():
     t = np.array([[1.0, 3.0, 3.0, 0.0], [2.0, 2.0, 2.0, 2.0]])
     assert O.verify_chain_greedy(t, [2]).tokens == [1]          # tie 1 vs 2 -> 1 wins
     assert O.verify_chain_greedy(t, [1]).tokens == [1, 0]       # accepted, bonus argmax 0
+
+
+# --- round termination: EOS and the length limit (KV4 §5) ---------------------------
+def _round(tokens, n_acc):
+    return O.ChainResult(n_acc=n_acc, tokens=list(tokens))
+
+
+def test_truncate_round_hand_cases():
+    r = _round([11, 12, 13, 99], 3)                 # three accepted drafts + a drawn token
+    t = O.truncate_round(r)
+    assert t.tokens == [11, 12, 13, 99] and t.n_acc == 3 and t.flags == 0
+    t = O.truncate_round(r, eos=12)                 # EOS among the accepted drafts
+    assert t.tokens == [11, 12] and t.n_acc == 2 and t.flags == O.FLAG_EOS
+    t = O.truncate_round(r, eos=99)                 # EOS is the drawn token: nothing cut
+    assert t.tokens == [11, 12, 13, 99] and t.n_acc == 3 and t.flags == O.FLAG_EOS
+    t = O.truncate_round(r, eos=7)                  # no EOS in the round
+    assert t.tokens == [11, 12, 13, 99] and t.flags == 0
+    t = O.truncate_round(r, max_new=2)              # two tokens left before the limit
+    assert t.tokens == [11, 12] and t.n_acc == 2 and t.flags == O.FLAG_LIMIT
+    t = O.truncate_round(r, max_new=4)              # the limit is not reached
+    assert t.tokens == [11, 12, 13, 99] and t.flags == 0
+    t = O.truncate_round(r, max_new=0)              # finished already
+    assert t.tokens == [] and t.n_acc == 0 and t.flags == O.FLAG_LIMIT
+    t = O.truncate_round(r, eos=13, max_new=2)      # the limit cuts before the EOS
+    assert t.tokens == [11, 12] and t.flags == O.FLAG_LIMIT
+    t = O.truncate_round(r, eos=12, max_new=3)      # the EOS cuts first
+    assert t.tokens == [11, 12] and t.flags == O.FLAG_EOS
+    t = O.truncate_round(_round([5], 0), eos=5)     # a rejection at once, the drawn token is EOS
+    assert t.tokens == [5] and t.n_acc == 0 and t.flags == O.FLAG_EOS
+    bad = O.ChainResult(flags=O.FLAG_BAD_INPUT)
+    assert O.truncate_round(bad, eos=1, max_new=0) is bad
+
+
+def test_truncate_round_properties():
+    """On random rounds: the result is the longest prefix of the round that
+    has no EOS before its last token and fits the limit, and n_acc counts the
+    drafts in it."""
+    rng = np.random.default_rng(3)
+    for _ in range(2000):
+        n_acc = int(rng.integers(0, 6))
+        toks = rng.integers(0, 6, n_acc + 1).tolist()
+        eos = int(rng.integers(0, 7)) if rng.random() < 0.8 else None
+        lim = int(rng.integers(-1, 8)) if rng.random() < 0.6 else None
+        t = O.truncate_round(_round(toks, n_acc), eos, lim)
+        L = len(t.tokens)
+        assert t.tokens == toks[:L]
+        assert eos is None or eos not in t.tokens[:-1]
+        assert lim is None or L <= max(lim, 0)
+        longer = toks[:L + 1]
+        if L < len(toks):
+            assert (eos is not None and eos in longer[:-1]) or (lim is not None and L + 1 > max(lim, 0))
+        assert t.n_acc == min(n_acc, L)
