@@ -71,6 +71,8 @@ extern "C" {
 #define SPEC_FLAG_TIMEOUT 8u    /* a bulk copy or a wait on other blocks' work did not complete
                                    within its limit (status word only): outputs of the call are
                                    not valid and the workspace must be zeroed again */
+#define SPEC_FLAG_EOS 16u       /* the round's output ends with the end-of-sequence token */
+#define SPEC_FLAG_LIMIT 32u     /* the round's output was cut at the request's length limit */
 
 /* workspace kinds for spec_workspace_bytes */
 #define SPEC_WS_CHAIN 0 /* n = gamma */
@@ -169,6 +171,17 @@ typedef struct SpecChainArgs {
     int32_t *blocks_in_use;     /* device out [B] or NULL (needs block_size >= 1) */
     int32_t block_size;         /* tokens per cache block, for blocks_in_use */
     int64_t kv_capacity;        /* positions a request's block table covers; 0 = unchecked */
+    /* Early end of the round ("KV Cache 优化（四）" §5: an EOS or the length
+     * limit ends a round before its 1..gamma+1 tokens).  The emitted tokens
+     * are cut right after the first eos_token (kept), then to max_new[b]
+     * tokens (a value <= 0 emits none); n_out is the cut length, n_acc the
+     * accepted drafts still emitted, out_tokens entries past n_out are -1
+     * where the round would have written them, and flags[b] gets
+     * SPEC_FLAG_EOS (the output ends with the EOS) / SPEC_FLAG_LIMIT (the
+     * limit cut it).  The in-place commit advances by the cut n_out. */
+    int32_t eos_enabled;        /* nonzero: cut after eos_token */
+    int32_t eos_token;          /* >= 0 when eos_enabled */
+    const int32_t *max_new;     /* device [B] or NULL */
 } SpecChainArgs;
 
 int spec_verify_chain(const SpecChainArgs *args, void *workspace, size_t workspace_bytes,

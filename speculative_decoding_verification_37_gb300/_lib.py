@@ -22,6 +22,7 @@ SPEC_DTYPE_BF16, SPEC_DTYPE_F32 = 0, 1
 SPEC_FLAG_BAD_INPUT, SPEC_FLAG_FALLBACK, SPEC_FLAG_BAD_ROW, SPEC_FLAG_TIMEOUT = 1, 2, 4, 8
 SPEC_WS_CHAIN, SPEC_WS_TREE, SPEC_WS_COMMIT, SPEC_WS_CHAIN_TOPK, SPEC_WS_CHAIN_FULL = 0, 1, 2, 3, 4
 SPEC_WS_TREE_LEVEL = 5
+SPEC_FLAG_EOS, SPEC_FLAG_LIMIT = 16, 32
 SPEC_TREE_MAX_HEADS = 64
 TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspace holds it
 
@@ -39,7 +40,8 @@ class SpecChainArgs(ctypes.Structure):
                 ("n_acc", c_void_p), ("out_tokens", c_void_p), ("n_out", c_void_p),
                 ("accept_prob", c_void_p), ("residual_mass", c_void_p), ("flags", c_void_p),
                 ("committed_len", c_void_p), ("draft_len", c_void_p), ("blocks_in_use", c_void_p),
-                ("block_size", c_int32), ("kv_capacity", c_int64)]
+                ("block_size", c_int32), ("kv_capacity", c_int64), ("eos_enabled", c_int32),
+                ("eos_token", c_int32), ("max_new", c_void_p)]
 
 
 class SpecTreeArgs(ctypes.Structure):
@@ -215,7 +217,8 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       committed_len: Optional[torch.Tensor] = None,
                       draft_len: Optional[torch.Tensor] = None,
                       blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
-                      kv_capacity: int = 0, stream=None) -> None:
+                      kv_capacity: int = 0, eos_token: Optional[int] = None,
+                      max_new: Optional[torch.Tensor] = None, stream=None) -> None:
     """Marshals one spec_verify_chain call.  Logits are 2-D [rows, V] views
     (row stride = stride(0)); every tensor must already be on the device."""
     V = target_logits.shape[-1]
@@ -231,7 +234,9 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       accept_prob=_ptr(accept_prob), residual_mass=_ptr(residual_mass),
                       flags=_ptr(flags), committed_len=_ptr(committed_len),
                       draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
-                      block_size=int(block_size), kv_capacity=int(kv_capacity))
+                      block_size=int(block_size), kv_capacity=int(kv_capacity),
+                      eos_enabled=0 if eos_token is None else 1,
+                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new))
     _check("spec_verify_chain", lib().spec_verify_chain(
         ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream)))
 
@@ -287,7 +292,8 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                              committed_len: Optional[torch.Tensor] = None,
                              draft_len: Optional[torch.Tensor] = None,
                              blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
-                             kv_capacity: int = 0, stream=None) -> None:
+                             kv_capacity: int = 0, eos_token: Optional[int] = None,
+                             max_new: Optional[torch.Tensor] = None, stream=None) -> None:
     """Marshals one spec_verify_chain_static call: the same as
     spec_verify_chain, but the library's fixed device array is the scratch,
     for callers that cannot allocate device memory."""
@@ -304,5 +310,7 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                       accept_prob=_ptr(accept_prob), residual_mass=_ptr(residual_mass),
                       flags=_ptr(flags), committed_len=_ptr(committed_len),
                       draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
-                      block_size=int(block_size), kv_capacity=int(kv_capacity))
+                      block_size=int(block_size), kv_capacity=int(kv_capacity),
+                      eos_enabled=0 if eos_token is None else 1,
+                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new))
     _check("spec_verify_chain_static", lib().spec_verify_chain_static(ctypes.byref(a), _stream(stream)))

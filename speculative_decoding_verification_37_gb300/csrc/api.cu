@@ -243,6 +243,8 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     if (a->draft_len && !a->committed_len) return SPEC_ERR_INVALID_ARG;
     if (a->kv_capacity < 0) return SPEC_ERR_INVALID_ARG;
     InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
+    if (a->eos_enabled && (a->eos_token < 0 || a->eos_token >= a->V)) return SPEC_ERR_INVALID_ARG;
+    const StopRule stop{a->eos_enabled ? a->eos_token : -1, a->max_new};
     const int64_t rows = (int64_t)a->B * (a->gamma + 1);
     if (!workspace || !aligned(workspace, 256) ||
         ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
@@ -276,6 +278,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.n_out = a->n_out;
         p.flags = a->flags;
         p.ip = ip;
+        p.stop = stop;
         if (rows * p.slices > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
         e = launch_argmax_verify(p, a->dtype, (int)rows, sm_count(), s);
     } else {
@@ -322,6 +325,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.qitem = w.qitem;
         p.qcap = (unsigned)(3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32));
         p.ip = ip;
+        p.stop = stop;
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
         // full vocabulary: the persistent kernel when the workspace, the
         // rows' alignment and the sizes allow it

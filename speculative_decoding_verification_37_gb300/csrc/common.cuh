@@ -276,6 +276,32 @@ __device__ __forceinline__ void inplace_commit(const IP &ip, int b, int len0, in
 
 // Sets a kernel's dynamic shared-memory limit once per device (the setting
 // is per device; doing it once keeps it out of captured launch sequences).
+// Early end of a chain round ("KV Cache 优化（四）" §5): the emitted tokens
+// are cut right after the first end-of-sequence token, then to the request's
+// remaining length.  stop_limit: the limit of request b (INT_MAX if none);
+// stop_scan: one 32-position chunk of the round (lane = position q, tok its
+// token, positions 0..n emitted before the cuts), updating `cut`, the first
+// EOS position seen (INT_MAX if none).
+template <typename SR> __device__ __forceinline__ int stop_limit(const SR &st, int b) {
+    if (!st.max_new) return 0x7fffffff;
+    const int m = st.max_new[b];
+    return m > 0 ? m : 0;
+}
+template <typename SR>
+__device__ __forceinline__ int stop_scan(const SR &st, int q0, int q, int n, int tok, int cut) {
+    const unsigned hit = __ballot_sync(kFull, st.eos >= 0 && q <= n && tok == st.eos);
+    return (cut == 0x7fffffff && hit) ? q0 + __ffs(hit) - 1 : cut;
+}
+// The round's emitted length after the cuts, and the flags that say which
+// cut shortened it (an EOS kept as the last token counts as an EOS end).
+__device__ __forceinline__ int stop_length(int n, int cut, int lim, unsigned &flags) {
+    const int L0 = cut < n ? cut + 1 : n + 1;  // n + 1 tokens unless an EOS comes first
+    const int L = L0 < lim ? L0 : lim;
+    if (cut <= n && cut < L) flags |= SPEC_FLAG_EOS;
+    if (lim < L0) flags |= SPEC_FLAG_LIMIT;
+    return L;
+}
+
 template <typename K>
 inline cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<unsigned long long> &done) {
     int dev = 0;

@@ -30,6 +30,12 @@ struct InPlace {
     int64_t capacity;  // 0 = unchecked
 };
 
+// Early end of a chain round at an end-of-sequence token or the length limit.
+struct StopRule {
+    int eos;             // < 0: none
+    const int *max_new;  // [B] tokens a request may still emit, or null
+};
+
 struct ArgmaxParams {
     const void *rows;
     int64_t stride;
@@ -50,6 +56,7 @@ struct ArgmaxParams {
     int *n_acc, *out_tokens, *n_out;
     unsigned *flags;
     InPlace ip;  // chain only
+    StopRule stop;
 };
 
 constexpr int kTopKFastMax = 128;  // top_k served by the candidate-list path
@@ -103,6 +110,7 @@ struct SampleParams {
     unsigned long long *qitem;   // [qcap] queue slots
     unsigned qcap;               // 3*B*(slices the workspace was sized for)
     InPlace ip;
+    StopRule stop;
 };
 
 constexpr int kTopKSlicePool = 256;  // candidates one slice of one row may hand on

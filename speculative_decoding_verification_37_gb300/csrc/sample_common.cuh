@@ -333,24 +333,30 @@ static __device__ void write_request_warp(const SampleParams &p, int b) {
     } else {
         int *out = p.out_tokens + (int64_t)b * (g + 1);
         const int *dt = p.tokens + (int64_t)b * g;
-        for (int q0 = 0; q0 <= g; q0 += 32) {
+        const int lim = stop_limit(p.stop, b);
+        int cut = 0x7fffffff;  // the first EOS position so far
+        unsigned fb = 0u;
+        for (int q0 = 0; q0 <= g; q0 += 32) {  // (uniform trip count: q0 <= g for every lane)
             const int q = q0 + lane;
-            if (q > g) break;
-            const PosRec r = q0 == 0 ? mine : load_rec(R + q);
-            if (q < n) out[q] = dt[q];
-            if (q == n) {
-                out[n] = r.token;
-                if (p.flags) p.flags[b] = (r.info & REC_FALLBACK) ? SPEC_FLAG_FALLBACK : 0u;
-            }
+            PosRec r{};
+            if (q <= g) r = q0 == 0 ? mine : load_rec(R + q);
+            const int tok = q < n ? dt[q] : (q == n ? r.token : -1);
+            cut = stop_scan(p.stop, q0, q, n, tok, cut);
+            if (q <= n) out[q] = (q < lim && q <= cut) ? tok : -1;
+            if (q == n && (r.info & REC_FALLBACK)) fb = SPEC_FLAG_FALLBACK;
             if (q < g) {
                 if (p.accept_prob) p.accept_prob[(int64_t)b * g + q] = r.a;
                 if (p.resid) p.resid[(int64_t)b * g + q] = r.z;
             }
         }
+        fb = __reduce_or_sync(kFull, fb);
         if (lane == 0) {
-            p.n_acc[b] = n;
-            p.n_out[b] = n + 1;
-            inplace_commit(p.ip, b, len0, n + 1);
+            unsigned f = fb;
+            const int L = stop_length(n, cut, lim, f);
+            p.n_acc[b] = n < L ? n : L;
+            p.n_out[b] = L;
+            if (p.flags) p.flags[b] = f;
+            inplace_commit(p.ip, b, len0, L);
         }
     }
     if (lane == 0) {

@@ -58,12 +58,21 @@ __device__ void greedy_chain_decide(const ArgmaxParams &p, int b) {
         }
     } else {
         int *out = p.out_tokens + (int64_t)b * (g + 1);
-        for (int k = lane; k <= n; k += 32) out[k] = k < n ? d[k] : argmax_key_index(keys[n]);
+        const int lim = stop_limit(p.stop, b);
+        int cut = 0x7fffffff;  // the first EOS position so far
+        for (int k0 = 0; k0 <= n; k0 += 32) {  // (n is warp-uniform)
+            const int k = k0 + lane;
+            const int tok = k < n ? d[k] : (k == n ? argmax_key_index(keys[n]) : -1);
+            cut = stop_scan(p.stop, k0, k, n, tok, cut);
+            if (k <= n) out[k] = (k < lim && k <= cut) ? tok : -1;
+        }
         if (lane == 0) {
-            p.n_acc[b] = n;
-            p.n_out[b] = n + 1;
-            if (p.flags) p.flags[b] = 0;
-            inplace_commit(p.ip, b, len0, n + 1);
+            unsigned f = 0u;
+            const int L = stop_length(n, cut, lim, f);
+            p.n_acc[b] = n < L ? n : L;
+            p.n_out[b] = L;
+            if (p.flags) p.flags[b] = f;
+            inplace_commit(p.ip, b, len0, L);
         }
     }
     __syncwarp();

@@ -56,6 +56,7 @@ def test_struct_layouts_match_c(lib):
         P(SpecTreeLevelArgs, flags) P(SpecTreeLevelArgs, next_row0)
         P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
         P(SpecChainArgs, committed_len) P(SpecChainArgs, block_size) P(SpecChainArgs, kv_capacity)
+        P(SpecChainArgs, eos_enabled) P(SpecChainArgs, max_new)
         P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
         P(SpecCommitArgs, flags) P(SpecCommitArgs, num_blocks) P(SpecCommitArgs, slots_stride)
         return 0;
@@ -108,6 +109,7 @@ def _chain_args(**over):
     dict(blocks_in_use=4096),                                   # needs committed_len
     dict(committed_len=4096, blocks_in_use=4352, block_size=0),  # needs block_size >= 1
     dict(draft_len=4096), dict(committed_len=4096, kv_capacity=-1),
+    dict(eos_enabled=1, eos_token=-1), dict(eos_enabled=1, eos_token=16),   # EOS outside [0, V)
 ])
 def test_chain_host_validation(lib, bad):
     a = _chain_args(**bad)
