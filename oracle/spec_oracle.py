@@ -77,11 +77,37 @@ def kept_set(logits: np.ndarray, top_k: int) -> np.ndarray:
     return x >= theta
 
 
-def transform_probs(logits: np.ndarray, temperature: float, top_k: int) -> Optional[np.ndarray]:
+def kept_set_top_p(probs: np.ndarray, top_p: float) -> np.ndarray:
+    """Boolean mask of the tokens top-p (nucleus) keeps from a distribution.
+
+    KV4 §4 names top-p among the transforms whose result enters the
+    acceptance rule; no page defines it further.  Reading: the smallest set
+    of the most probable tokens whose total probability reaches top_p, with
+    every token tied with the least probable kept one also kept (the same
+    tie rule as top-k).  top_p >= 1 keeps every token.
+    """
+    p = np.asarray(probs, dtype=np.float64)
+    if top_p >= 1.0:
+        return np.ones(p.shape[0], dtype=bool)
+    order = np.argsort(-p, kind="stable")
+    mass = 0.0
+    last = p[order[0]]
+    for i in order:
+        mass += p[i]
+        last = p[i]
+        if mass >= top_p:
+            break
+    return p >= last
+
+
+def transform_probs(logits: np.ndarray, temperature: float, top_k: int,
+                    top_p: float = 1.0) -> Optional[np.ndarray]:
     """p_i = exp((l_i - m)/T) / sum_{j kept} exp((l_j - m)/T) for kept i, else 0.
 
-    m is the largest kept logit.  Returns None when every kept logit is -inf
-    (the row defines no distribution).
+    m is the largest kept logit.  With top_p < 1 the result is then cut to
+    its nucleus (kept_set_top_p) and renormalised (reading: temperature, then
+    top-k, then top-p).  Returns None when every kept logit is -inf (the row
+    defines no distribution).
     """
     x = np.asarray(logits, dtype=np.float64)
     keep = kept_set(x, top_k)
@@ -90,7 +116,11 @@ def transform_probs(logits: np.ndarray, temperature: float, top_k: int) -> Optio
         return None
     e = np.zeros_like(x)
     e[keep] = np.exp((x[keep] - m) / temperature)
-    return e / e.sum()
+    p = e / e.sum()
+    if top_p < 1.0:
+        p = np.where(kept_set_top_p(p, top_p), p, 0.0)
+        p = p / p.sum()
+    return p
 
 
 def greedy_argmax(logits: np.ndarray) -> int:
@@ -161,8 +191,11 @@ class ChainResult:
 
 def verify_chain_sampled(target: np.ndarray, draft: np.ndarray, draft_tokens: np.ndarray,
                          uniforms: np.ndarray, temperature: float, top_k: int = 0,
-                         eps: float = DEFAULT_EPS, margin: float = BOUNDARY_MARGIN) -> ChainResult:
-    """One speculative-sampling round of one request.
+                         eps: float = DEFAULT_EPS, margin: float = BOUNDARY_MARGIN,
+                         top_p: float = 1.0) -> ChainResult:
+    """One speculative-sampling round of one request (top_p < 1: the nucleus
+    transform too, on both sides, as KV4 §4 asks of every processed
+    distribution).
 
     target: [gamma+1, V] logits (p_1..p_{gamma+1}); draft: [gamma, V] logits
     (q_1..q_gamma); draft_tokens: d_1..d_gamma; uniforms: u[0..gamma-1] for the
@@ -185,8 +218,8 @@ def verify_chain_sampled(target: np.ndarray, draft: np.ndarray, draft_tokens: np
     if any(t < 0 or t >= V for t in d):
         res.flags |= FLAG_BAD_INPUT
         return res
-    P = [transform_probs(target[k], temperature, top_k) for k in range(gamma + 1)]
-    Q = [transform_probs(draft[k], temperature, top_k) for k in range(gamma)]
+    P = [transform_probs(target[k], temperature, top_k, top_p) for k in range(gamma + 1)]
+    Q = [transform_probs(draft[k], temperature, top_k, top_p) for k in range(gamma)]
     if any(x is None for x in P) or any(x is None for x in Q):
         res.flags |= FLAG_BAD_ROW
         return res

@@ -285,3 +285,68 @@ def test_truncate_round_properties():
         if L < len(toks):
             assert (eos is not None and eos in longer[:-1]) or (lim is not None and L + 1 > max(lim, 0))
         assert t.n_acc == min(n_acc, L)
+
+
+# --- top-p (nucleus) transform: a reading of KV4 §4 -----------------------------------
+def test_top_p_hand_cases():
+    p = np.array([0.5, 0.125, 0.25, 0.125])           # dyadic: sums are exact
+    assert O.kept_set_top_p(p, 0.5).tolist() == [True, False, False, False]
+    assert O.kept_set_top_p(p, 0.75).tolist() == [True, False, True, False]
+    # 0.76 needs a third token; the fourth is tied with it and is kept too
+    assert O.kept_set_top_p(p, 0.76).tolist() == [True, True, True, True]
+    assert O.kept_set_top_p(p, 1.0).all() and O.kept_set_top_p(p, 1e-9).tolist() == [True, False, False, False]
+
+
+def test_top_p_after_temperature_and_top_k():
+    x = np.array([2.0, 1.0, 0.0, -1.0])
+    # T = 1: the top token has 0.64 < 0.85, so two are kept; T = 0.5 sharpens
+    # the row to 0.87 for the top token, which alone reaches 0.85
+    assert (O.transform_probs(x, 1.0, 0, 0.85) > 0).tolist() == [True, True, False, False]
+    assert (O.transform_probs(x, 0.5, 0, 0.85) > 0).tolist() == [True, False, False, False]
+    # top-k first: with k = 2 the two kept tokens renormalise to 0.73 / 0.27,
+    # so top-p 0.7 keeps one of them
+    assert (O.transform_probs(x, 1.0, 2, 0.7) > 0).tolist() == [True, False, False, False]
+    p = O.transform_probs(x, 1.0, 0, 0.85)
+    assert p.sum() == pytest.approx(1.0) and p[0] / p[1] == pytest.approx(np.e)
+
+
+def test_top_p_properties_random():
+    """Any row: the kept mass reaches top_p, dropping the least probable kept
+    tie group falls short of it, and every token more probable than a kept
+    one is kept."""
+    rng = np.random.default_rng(11)
+    for _ in range(500):
+        V = int(rng.integers(1, 30))
+        p = rng.dirichlet(np.ones(V) * rng.choice([0.2, 1.0, 5.0]))
+        if rng.random() < 0.3:
+            p = np.round(p * 8) / 8 + 1e-3                 # planted ties
+            p /= p.sum()
+        tp = float(rng.uniform(0.01, 0.999))
+        keep = O.kept_set_top_p(p, tp)
+        assert p[keep].sum() >= tp - 1e-12
+        low = p[keep].min()
+        assert p[keep & (p > low)].sum() < tp
+        assert not (~keep & (p > low)).any()
+
+
+def test_sampled_round_with_top_p_keeps_losslessness():
+    """With the nucleus transform on both sides, the round's output
+    distribution is still the target's (transformed) distribution: the
+    brute-force enumeration of every draft and uniform region."""
+    rng = np.random.default_rng(2)
+    V, T, tp = 4, 1.0, 0.8
+    tgt = rng.normal(0, 1, (2, V))
+    drf = rng.normal(0, 1, (1, V))
+    p = O.transform_probs(tgt[0], T, 0, tp)
+    q = O.transform_probs(drf[0], T, 0, tp)
+    out = np.zeros(V)
+    grid = (np.arange(160) + 0.5) / 160
+    for d in range(V):
+        if q[d] == 0:
+            continue
+        for u0 in grid:
+            for u1 in grid:
+                r = O.verify_chain_sampled(tgt, drf, np.array([d]), np.array([u0, u1]), T, 0,
+                                           top_p=tp)
+                out[r.tokens[0]] += q[d] / grid.size ** 2
+    assert np.abs(out - p).max() < 1e-2
