@@ -182,6 +182,16 @@ typedef struct SpecChainArgs {
     int32_t eos_enabled;        /* nonzero: cut after eos_token */
     int32_t eos_token;          /* >= 0 when eos_enabled */
     const int32_t *max_new;     /* device [B] or NULL */
+    /* top-p ("KV Cache 优化（四）" §4 names top-p among the processed
+     * distributions that enter the acceptance rule): with 0 < top_p < 1,
+     * after temperature and top-k each row keeps the smallest set of its
+     * most probable tokens whose probability reaches top_p (tokens tied with
+     * the least probable kept one are kept too), renormalised; target and
+     * draft alike.  Needs 1 <= top_k <= 128 and a workspace of
+     * SPEC_WS_CHAIN_TOPK size (SPEC_ERR_UNSUPPORTED otherwise).  A position
+     * whose kept set has more than 256 tied logits is flagged
+     * SPEC_FLAG_BAD_ROW.  0 (the zeroed default) or >= 1: off. */
+    float top_p;
 } SpecChainArgs;
 
 int spec_verify_chain(const SpecChainArgs *args, void *workspace, size_t workspace_bytes,

@@ -41,7 +41,7 @@ class SpecChainArgs(ctypes.Structure):
                 ("accept_prob", c_void_p), ("residual_mass", c_void_p), ("flags", c_void_p),
                 ("committed_len", c_void_p), ("draft_len", c_void_p), ("blocks_in_use", c_void_p),
                 ("block_size", c_int32), ("kv_capacity", c_int64), ("eos_enabled", c_int32),
-                ("eos_token", c_int32), ("max_new", c_void_p)]
+                ("eos_token", c_int32), ("max_new", c_void_p), ("top_p", c_float)]
 
 
 class SpecTreeArgs(ctypes.Structure):
@@ -218,7 +218,8 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       draft_len: Optional[torch.Tensor] = None,
                       blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
                       kv_capacity: int = 0, eos_token: Optional[int] = None,
-                      max_new: Optional[torch.Tensor] = None, stream=None) -> None:
+                      max_new: Optional[torch.Tensor] = None, top_p: float = 0.0,
+                      stream=None) -> None:
     """Marshals one spec_verify_chain call.  Logits are 2-D [rows, V] views
     (row stride = stride(0)); every tensor must already be on the device."""
     V = target_logits.shape[-1]
@@ -236,7 +237,8 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
                       block_size=int(block_size), kv_capacity=int(kv_capacity),
                       eos_enabled=0 if eos_token is None else 1,
-                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new))
+                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new),
+                      top_p=float(top_p))
     _check("spec_verify_chain", lib().spec_verify_chain(
         ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream)))
 
@@ -293,7 +295,8 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                              draft_len: Optional[torch.Tensor] = None,
                              blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
                              kv_capacity: int = 0, eos_token: Optional[int] = None,
-                             max_new: Optional[torch.Tensor] = None, stream=None) -> None:
+                             max_new: Optional[torch.Tensor] = None, top_p: float = 0.0,
+                             stream=None) -> None:
     """Marshals one spec_verify_chain_static call: the same as
     spec_verify_chain, but the library's fixed device array is the scratch,
     for callers that cannot allocate device memory."""
@@ -312,5 +315,6 @@ def spec_verify_chain_static(*, target_logits: torch.Tensor, draft_tokens: torch
                       draft_len=_ptr(draft_len), blocks_in_use=_ptr(blocks_in_use),
                       block_size=int(block_size), kv_capacity=int(kv_capacity),
                       eos_enabled=0 if eos_token is None else 1,
-                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new))
+                      eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new),
+                      top_p=float(top_p))
     _check("spec_verify_chain_static", lib().spec_verify_chain_static(ctypes.byref(a), _stream(stream)))

@@ -57,7 +57,8 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                  draft_len: Optional[torch.Tensor] = None,
                  blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
                  kv_capacity: int = 0, eos_token: Optional[int] = None,
-                 max_new: Optional[torch.Tensor] = None, stream=None) -> ChainOut:
+                 max_new: Optional[torch.Tensor] = None, top_p: float = 0.0,
+                 stream=None) -> ChainOut:
     """target [B*(gamma+1), V], draft [B*gamma, V] (bf16 or f32, rows may be
     strided), draft_tokens int32 [B, gamma], uniforms f32 [B, gamma+1].
 
@@ -66,7 +67,8 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
     draft_len (if given) is cut back to it and blocks_in_use (if given)
     follows, all on the device.  eos_token / max_new (int32 [B] on the
     device) end the round early: its output is cut right after the first
-    EOS, then to max_new[b] tokens."""
+    EOS, then to max_new[b] tokens.  0 < top_p < 1 adds the nucleus after
+    top-k (needs 1 <= top_k <= 128)."""
     dev = target.device
     V = target.shape[-1]
     B = target.shape[0] // (gamma + 1)
@@ -91,7 +93,7 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                         committed_len=committed_len, draft_len=draft_len,
                         blocks_in_use=blocks_in_use, block_size=block_size,
                         kv_capacity=kv_capacity, eos_token=eos_token, max_new=max_new,
-                        stream=stream)
+                        top_p=top_p, stream=stream)
     return out
 
 

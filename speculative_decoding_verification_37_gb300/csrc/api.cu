@@ -245,6 +245,8 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
     if (a->eos_enabled && (a->eos_token < 0 || a->eos_token >= a->V)) return SPEC_ERR_INVALID_ARG;
     const StopRule stop{a->eos_enabled ? a->eos_token : -1, a->max_new};
+    if (!(a->top_p >= 0.0f) || !std::isfinite(a->top_p)) return SPEC_ERR_INVALID_ARG;
+    const bool nucleus = a->top_p > 0.0f && a->top_p < 1.0f && !greedy;
     const int64_t rows = (int64_t)a->B * (a->gamma + 1);
     if (!workspace || !aligned(workspace, 256) ||
         ws_bytes < spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V))
@@ -300,6 +302,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.exptab = exp_tables();
         split(1.0 / (double)a->temperature, p.exptab.it);
         p.top_k = (a->top_k >= a->V) ? 0 : a->top_k;
+        p.top_p = nucleus ? a->top_p : 0.0f;
         p.eps = a->fallback_eps;
         p.n_acc = a->n_acc;
         p.out_tokens = a->out_tokens;
@@ -332,7 +335,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         const int64_t rbytes = (int64_t)a->V * (int64_t)es;
         // (small calls stay on the cluster kernel: a whole-GPU cooperative
         // grid only pays off with a few thousand slices of work)
-        const bool full = has_full && p.top_k == 0 && !a->residual_mass && a->gamma <= 30 &&
+        const bool full = !nucleus && has_full && p.top_k == 0 && !a->residual_mass && a->gamma <= 30 &&
                           rows * full_slices(a->V, a->dtype) >= 1024 &&
                           rbytes % 16 == 0 && rbytes <= (int64_t)full_row_bytes() * full_max_slices() &&
                           aligned(a->target_logits, 16) && (a->target_row_stride * (int64_t)es) % 16 == 0 &&
@@ -352,6 +355,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         const int cf = topk_slices(a->V, a->dtype);
         const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax &&
                           (int64_t)cf * (p.top_k + 16) <= kTopKMerge;
+        if (nucleus && !fast) return SPEC_ERR_UNSUPPORTED;  // the nucleus is built in the top-k merge
         if (fast) {
             p.c = cf;
             p.Vs = slice_len(a->V, cf);

@@ -85,6 +85,7 @@ struct SampleParams {
     float c2lo;    // its rounding residue: c2 + c2lo = log2(e) / temperature to ~2^-48
     DdExpTables exptab;   // 1/T, ln2/64 in parts, 2^(j/64): the double-float exponential
     int top_k;     // 0 = keep all
+    float top_p;   // nucleus after top-k when in (0, 1); otherwise off
     float eps;
     int *n_acc, *out_tokens, *n_out;
     float *accept_prob, *resid;

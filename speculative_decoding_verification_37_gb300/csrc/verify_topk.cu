@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
             int kn = 0;
             uint2 *tmp = cand + ncu;
             const int cap2 = cap - ncu;
-            const uint32_t th = warp_kth_entries(cand, ncu, min(K, (unsigned)ncu));
+            uint32_t th = warp_kth_entries(cand, ncu, min(K, (unsigned)ncu));
             for (int x0 = 0; x0 < ncu; x0 += 32) {
                 const int x = x0 + lane;
                 const bool keep = x < ncu && cand[x].x >= th;
@@ -706,6 +706,62 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
                         S = dd_add(S, dd_expw(key_value<T>(s_kept[r][x].x), m, EK));
                 }
                 S = warp_dd_sum(S);
+                if (p.top_p > 0.0f && p.top_p < 1.0f && m != -INFINITY) {
+                    // the nucleus of the kept set: its entries by probability
+                    // (larger key first, then the lower token), the first rank
+                    // whose cumulative probability reaches top_p, and every
+                    // entry at or above that rank's key (ties kept), still in
+                    // token order; the row's sum is taken again over them
+                    uint2 *srt = L;                                          // [kn] by rank
+                    float2 *prb = reinterpret_cast<float2 *>(L + kKeptMax);  // [kn] by rank
+                    const dd iS = dd_recip(S);
+                    for (int x = lane; x < kn; x += 32) {
+                        const uint2 e = s_kept[r][x];
+                        int rank = 0;
+                        for (int y = 0; y < kn; ++y) {
+                            const uint2 f = s_kept[r][y];
+                            rank += f.x > e.x || (f.x == e.x && f.y < e.y);
+                        }
+                        srt[rank] = e;
+                        const dd pe = dd_mul(dd_expw(key_value<T>(e.x), m, EK), iS);
+                        prb[rank] = make_float2(pe.hi, pe.lo);
+                    }
+                    __syncwarp();
+                    const int E = (kn + 31) / 32, i0 = lane * E, i1 = min(kn, i0 + E);
+                    dd part{0.0f, 0.0f};
+                    for (int i = i0; i < i1; ++i) part = dd_add(part, dd{prb[i].x, prb[i].y});
+                    dd cum = warp_dd_excl_scan(part);
+                    const dd tp{p.top_p, 0.0f};
+                    int cut = INT_MAX;
+                    for (int i = i0; i < i1; ++i) {
+                        cum = dd_add(cum, dd{prb[i].x, prb[i].y});
+                        if (!dd_gt(tp, cum)) {  // cumulative probability >= top_p
+                            cut = i;
+                            break;
+                        }
+                    }
+                    cut = (int)__reduce_min_sync(kFull, (unsigned)cut);
+                    if (cut == INT_MAX) cut = kn - 1;  // rounding left the total below top_p
+                    const uint32_t kstar = srt[cut].x;
+                    int nn = 0;
+                    for (int x0 = 0; x0 < kn; x0 += 32) {
+                        const int x = x0 + lane;
+                        const uint2 e = x < kn ? s_kept[r][x] : make_uint2(0u, 0u);
+                        const bool keep = x < kn && e.x >= kstar;
+                        const unsigned bal = __ballot_sync(kFull, keep);
+                        __syncwarp();  // every lane has read its entry before any is moved
+                        if (keep) s_kept[r][nn + __popc(bal & lt)] = e;
+                        nn += __popc(bal);
+                    }
+                    __syncwarp();
+                    kn = nn;
+                    th = kstar;
+                    S = dd{0.0f, 0.0f};
+#pragma unroll 1
+                    for (int x = lane; x < kn; x += 32)
+                        S = dd_add(S, dd_expw(key_value<T>(s_kept[r][x].x), m, EK));
+                    S = warp_dd_sum(S);
+                }
                 if (lane == 0) {
                     s_m[r] = m;
                     s_S[r] = make_float2(S.hi, S.lo);
@@ -720,6 +776,14 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_merge_kernel(SampleParams p
         __syncthreads();
     }
     if (s_bad) {
+        if (p.top_p > 0.0f && p.top_p < 1.0f) {
+            // the masked path has no nucleus: the position is flagged
+            if (wid == 0) {
+                Outcome o{1.0f, 0.0f, -1, REC_BAD_ROW};
+                finish(p, b, k, o, sb);
+            }
+            return;
+        }
         // an overflowed or poisoned slice, or hundreds of logits tied at the
         // threshold: the exact masked path over the whole rows
         SoloEx solo;

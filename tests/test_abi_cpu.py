@@ -56,7 +56,7 @@ def test_struct_layouts_match_c(lib):
         P(SpecTreeLevelArgs, flags) P(SpecTreeLevelArgs, next_row0)
         P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
         P(SpecChainArgs, committed_len) P(SpecChainArgs, block_size) P(SpecChainArgs, kv_capacity)
-        P(SpecChainArgs, eos_enabled) P(SpecChainArgs, max_new)
+        P(SpecChainArgs, eos_enabled) P(SpecChainArgs, max_new) P(SpecChainArgs, top_p)
         P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
         P(SpecCommitArgs, flags) P(SpecCommitArgs, num_blocks) P(SpecCommitArgs, slots_stride)
         return 0;
@@ -110,6 +110,7 @@ def _chain_args(**over):
     dict(committed_len=4096, blocks_in_use=4352, block_size=0),  # needs block_size >= 1
     dict(draft_len=4096), dict(committed_len=4096, kv_capacity=-1),
     dict(eos_enabled=1, eos_token=-1), dict(eos_enabled=1, eos_token=16),   # EOS outside [0, V)
+    dict(top_p=-0.5), dict(top_p=float("nan")),
 ])
 def test_chain_host_validation(lib, bad):
     a = _chain_args(**bad)
@@ -198,3 +199,14 @@ def test_tree_level_children_limits(lib):
     assert lib.spec_tree_level(ctypes.byref(a), ctypes.c_void_p(4096), 64, None) == L.SPEC_ERR_INVALID_ARG
     assert lib.spec_tree_level(ctypes.byref(_level_args(B=0)), None, 0, None) == L.SPEC_OK
     assert L.spec_workspace_bytes(L.SPEC_WS_TREE_LEVEL, 128, 2, 128256) >= 128 * 2 * 32 * 144
+
+
+def test_top_p_needs_the_top_k_path(lib):
+    """The nucleus is built in the top-k merge: top_p without 1 <= top_k <= 128
+    is refused before anything is launched."""
+    for top_k in (0, 129):
+        a = _chain_args(top_p=0.9, top_k=top_k)
+        n = L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 2, 2, 16)
+        ws = ctypes.create_string_buffer(n + 256)
+        base = (ctypes.addressof(ws) + 255) // 256 * 256
+        assert lib.spec_verify_chain(ctypes.byref(a), ctypes.c_void_p(base), n, None) == L.SPEC_ERR_UNSUPPORTED
