@@ -109,12 +109,13 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = None
 
     def start(self):
+        import tempfile
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{self.gpu}_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv",
                  "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -133,14 +134,16 @@ class ClockSampler:
         self.fh.close()
         rows = []
         with open(self.path) as f:
-            for line in f.read().splitlines()[1:]:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts[5:9]))
-                except ValueError:
-                    continue
+            text = f.read()
+        os.unlink(self.path)  # the summary below goes into the JSON line
+        for line in text.splitlines()[1:]:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts[5:9]))
+            except ValueError:
+                continue
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -158,7 +161,7 @@ class Workload:
     def __init__(self, cfg: int, seed: int, device, batch=None):
         import dataclasses
         self.cfg = cfg
-        self.spec = W.CONFIGS[cfg] if not batch else dataclasses.replace(W.CONFIGS[cfg], B=batch)
+        self.spec = W.WORKLOADS[cfg] if not batch else dataclasses.replace(W.WORKLOADS[cfg], B=batch)
         self.device = device
         s = self.spec
         if isinstance(s, W.TreeSpec):
@@ -350,7 +353,7 @@ def oracle_sample(cfg: int, seconds: float = 12.0, seed: int = 0, n_gen: int = 1
     about `seconds` (or the wall clock reaches `wall_cap`).  Returns
     (rows/s, sample text, requests run)."""
     import oracle as O
-    spec = W.CONFIGS[cfg]
+    spec = W.WORKLOADS[cfg]
     reqs = list(range(min(spec.B, n_gen)))
     if isinstance(spec, W.TreeSpec):
         tb = W.make_tree(spec, seed=seed, requests=reqs)
@@ -436,7 +439,7 @@ def barrier(world: int):
 
 def config_dict(cfg: int, world: int, batch: int = 0):
     import dataclasses
-    s = W.CONFIGS[cfg] if not batch else dataclasses.replace(W.CONFIGS[cfg], B=batch)
+    s = W.WORKLOADS[cfg] if not batch else dataclasses.replace(W.WORKLOADS[cfg], B=batch)
     d = {"workload": s.name, "B_per_gpu": s.B, "V": s.V, "dtype": s.dtype,
          "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
          "parallelism": f"dp{world} (independent request shards, no collective)"}
@@ -454,7 +457,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     v, sample, _ = oracle_sample(args.config, seconds=max(2.0, 4.0 * args.steps))
-    s = W.CONFIGS[args.config]
+    s = W.WORKLOADS[args.config]
     dtype = s.dtype
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
@@ -583,7 +586,7 @@ def run_tree_build(args, rank, world, local):
     three level calls of a whole tree (captured in one CUDA graph), the draft
     rows resident; L2 flushed between steps."""
     import dataclasses
-    spec = W.CONFIGS[4] if not args.batch else dataclasses.replace(W.CONFIGS[4], B=args.batch)
+    spec = W.WORKLOADS[4] if not args.batch else dataclasses.replace(W.WORKLOADS[4], B=args.batch)
     levels = W.make_tree_levels(spec, seed=rank)
     logit_bytes = sum(lv.numel() * lv.element_size() for lv in levels)
     cfg = {"workload": f"tree build {[list(k) for k in spec.topKSpec]}/{list(spec.topHead)} "
@@ -866,7 +869,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_max, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": W.CONFIGS[args.config].dtype, "data": "synthetic",
+                "dtype": W.WORKLOADS[args.config].dtype, "data": "synthetic",
                 "config": config_dict(args.config, world, args.batch),
                 "rounds_per_s": wl.B * world / (t_step_max * 1e-3),
                 "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /

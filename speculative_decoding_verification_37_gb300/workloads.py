@@ -135,7 +135,7 @@ class TreeSpec:
 
 
 # The five workloads the verify-and-commit step is specified on.
-CONFIGS = {
+WORKLOADS = {
     1: ChainSpec("chain-tiny B=8 g=4 V=1024 f32 T=1", B=8, gamma=4, V=1024, dtype="f32",
                  target_sigma=2.0, draft_sigma=0.7, temperature=1.0),
     2: ChainSpec("chain B=64 g=4 V=128256 bf16 T=0.8 top-k=50 + KV commit", B=64, gamma=4,
@@ -432,7 +432,7 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = [
-    "KVSpec", "ChainSpec", "TreeSpec", "CONFIGS", "ChainBatch", "make_chain", "DraftTree",
+    "KVSpec", "ChainSpec", "TreeSpec", "WORKLOADS", "ChainBatch", "make_chain", "DraftTree",
     "grow_tree", "TreeBatch", "make_tree", "KVBatch", "make_kv", "make_cache",
     "uniforms24", "KV_SENTINEL",
 ]

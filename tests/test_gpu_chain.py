@@ -49,7 +49,7 @@ def test_sampled_chain_matches_oracle(case):
 
 
 def test_sampled_chain_zipf_topk_config_like():
-    s = dataclasses.replace(W.CONFIGS[2], B=6)
+    s = dataclasses.replace(W.WORKLOADS[2], B=6)
     batch = W.make_chain(s, seed=5)
     compare_chain(batch, run_chain(batch), range(batch.n))
 

@@ -73,7 +73,7 @@ def test_full_path_matches_oracle(case):
 
 def test_full_path_large_f32_rows():
     """The 128,256-token fp32 rows of the large chain workload, 24 requests."""
-    s = W.CONFIGS[5]
+    s = W.WORKLOADS[5]
     batch = W.make_chain(W.ChainSpec("t", B=24, gamma=s.gamma, V=s.V, dtype=s.dtype,
                                      target_sigma=s.target_sigma, temperature=s.temperature,
                                      top_k=0, draft_sigma=s.draft_sigma, equal_rows_frac=0.05), seed=11)

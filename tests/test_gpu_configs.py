@@ -53,7 +53,7 @@ def commit_and_check(kvb: W.KVBatch, n_slots, slots=None):
 
 
 def check_chain_config(cfg, residual=True):
-    spec = W.CONFIGS[cfg]
+    spec = W.WORKLOADS[cfg]
     batch = W.make_chain(spec, seed=0)
     gpu = run_chain(batch, residual=residual)
     tally = compare_chain(batch, gpu, range(batch.n))
@@ -81,7 +81,7 @@ def test_config3_greedy_chain_bit_exact():
 
 
 def test_config4_tree_and_commit():
-    spec = W.CONFIGS[4]
+    spec = W.WORKLOADS[4]
     tb = W.make_tree(spec, seed=0)
     kvb = W.make_kv(spec.kv, spec.B, spec.n_nodes + 1, seed=0)
     d = "cuda"
@@ -117,7 +117,7 @@ def test_config5_chain_f32_equal_rows_and_commit():
 def test_boundary_case_rate_on_many_decisions():
     """Config-1 shapes with 4096 requests: boundary cases stay under 1e-4 of
     the decisions."""
-    spec = dataclasses.replace(W.CONFIGS[1], B=4096)
+    spec = dataclasses.replace(W.WORKLOADS[1], B=4096)
     batch = W.make_chain(spec, seed=1)
     gpu = run_chain(batch, residual=False)
     t = compare_chain(batch, gpu, range(batch.n), ChainTally())

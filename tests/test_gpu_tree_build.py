@@ -75,7 +75,7 @@ def random_levels(B, V, topHead, dtype, seed, sigma=3.0, quant=None):
 
 
 def test_page_shape_large_rows_bf16():
-    s = dataclasses.replace(W.CONFIGS[4], B=24)
+    s = dataclasses.replace(W.WORKLOADS[4], B=24)
     levels = W.make_tree_levels(s, seed=3)
     gpu, _ = build_gpu(levels, s.topKSpec, s.topHead, s.V)
     trees = oracle_trees(levels, s.topKSpec, s.topHead, range(s.B))
@@ -151,7 +151,7 @@ def test_strided_misaligned_rows_and_repeat_calls():
 def test_built_tree_feeds_the_tree_verify():
     """The builder's node arrays are the tree verify's input layout: verify
     the GPU-built trees against target rows and compare with the oracle."""
-    s = dataclasses.replace(W.CONFIGS[4], B=16, V=20000)
+    s = dataclasses.replace(W.WORKLOADS[4], B=16, V=20000)
     levels = W.make_tree_levels(s, seed=2)
     gpu, tb = build_gpu(levels, s.topKSpec, s.topHead, s.V)
     target = W.make_tree(s, seed=2).logits
@@ -167,7 +167,7 @@ def test_built_tree_feeds_the_tree_verify():
 
 def test_large_batch_sampled():
     """The full 128-request workload, 24 requests compared."""
-    s = W.CONFIGS[4]
+    s = W.WORKLOADS[4]
     levels = W.make_tree_levels(s, seed=0)
     gpu, _ = build_gpu(levels, s.topKSpec, s.topHead, s.V)
     reqs = list(range(0, s.B, 6))[:24]

@@ -35,7 +35,7 @@ def _outputs(B, g, sampled, dev):
 CASES = {
     "topk": W.ChainSpec("topk", B=16, gamma=4, V=128256, dtype="bf16", target_sigma=3.0,
                         zipf_bias=True, draft_sigma=1.0, temperature=0.8, top_k=50),
-    "full": W.CONFIGS[1],
+    "full": W.WORKLOADS[1],
     "greedy": W.ChainSpec("greedy", B=32, gamma=8, V=152064, dtype="bf16", target_sigma=3.0,
                           temperature=0.0),
 }
