@@ -18,7 +18,13 @@
  *     ancestors only and its position id is its depth.
  *   * "KV Cache 优化（四）" §6 and §10.6.3: the accepted prefix's temporary
  *     K/V is committed at one boundary in every layer, the commit length
- *     advances, rejected slots are rolled back without copying blocks.
+ *     advances, rejected slots are rolled back without copying blocks (or,
+ *     with reserved slots, the verify call advances the length in place).
+ *   * Options of the chain call: top-p after top-k (§4 names it), the early
+ *     end of a round at EOS or the length limit (§5).
+ *   * The draft side: one level of a topKSpec/topHead draft tree per
+ *     spec_tree_level call ("投机推理" 树形投机怎么配置), and prompt-lookup
+ *     drafts from the token history (spec_ngram_draft; §10.6.3 实际部署).
  *
  * Conventions for every entry point
  *   * All pointers named "device" are CUDA device (or managed) pointers; the
@@ -35,8 +41,9 @@
  *     are found on the device: the request's flags word and the workspace's
  *     sticky status word get a SPEC_FLAG_* bit, the request's outputs are
  *     not written except n_acc = n_out = 0 (and for a commit, nothing is
- *     copied and its length does not advance).  No kernel traps or waits on
- *     another block.
+ *     copied and its length does not advance).  No kernel traps; every wait
+ *     on another block's work or on a bulk copy is bounded, and one that
+ *     runs out sets SPEC_FLAG_TIMEOUT in the status word.
  *   * Logits must not contain NaN or +inf (-inf is allowed and means "never").
  *   * The workspace must be at least spec_workspace_bytes(...) bytes, 256-byte
  *     aligned and zero-filled before its first use; every call leaves it
