@@ -176,3 +176,19 @@ def test_host_generator_grows_the_oracle_tree(seed):
     np.testing.assert_array_equal(g.node_token, t.node_token)
     np.testing.assert_array_equal(g.node_parent, t.node_parent)
     np.testing.assert_array_equal(g.row_of_node, t.row_of_node)
+
+
+def test_level_rows_are_the_tree_workloads_draft_rows():
+    """make_tree_levels gives, level by level, the draft rows make_tree grows
+    its trees from (f32, so no rounding between the two): the oracle's build
+    from them is make_tree's tree."""
+    import dataclasses
+    s = dataclasses.replace(W.WORKLOADS[4], B=3, V=700, dtype="f32")
+    levels = W.make_tree_levels(s, seed=6)
+    tb = W.make_tree(s, seed=6)
+    for b in range(s.B):
+        rows = [lv[b * h:(b + 1) * h].double().numpy() for lv, h in zip(levels, s.topHead)]
+        t = O.build_tree(rows, s.topKSpec, s.topHead)
+        np.testing.assert_array_equal(t.node_token, tb.node_token[b])
+        np.testing.assert_array_equal(t.node_parent, tb.node_parent[b])
+        np.testing.assert_array_equal(t.row_of_node, tb.row_of_node[b])
