@@ -369,6 +369,34 @@ def verify_tree(logits: np.ndarray, node_token: np.ndarray, node_parent: np.ndar
     return res
 
 
+def verify_chain_batch(target: np.ndarray, draft: np.ndarray, draft_tokens: np.ndarray,
+                       uniforms: np.ndarray, gammas, temperatures, top_ks, top_ps=None):
+    """A batch whose requests each have their own gamma, temperature, top-k
+    and top-p ([LLMI §10.6.3]: requests in one batch accept different
+    lengths and start the next step at different points; per-request
+    sampling settings follow the same rule per request, [KV4 §4]).
+
+    Layout reading: the arrays are padded to gamma_max = draft_tokens.shape[1]:
+    target [B, gamma_max+1, V], draft [B, gamma_max, V], uniforms
+    [B, gamma_max+1]; request b uses target rows 0..gamma_b, draft rows and
+    tokens 0..gamma_b-1, accept uniforms u[b][0..gamma_b-1] and u[b][gamma_b]
+    for its final draw.  Temperature 0 means greedy for that request.  Each
+    request is one call of the single-request rule on its own slice."""
+    out = []
+    B = draft_tokens.shape[0]
+    for b in range(B):
+        g = int(gammas[b])
+        T = float(temperatures[b])
+        if T == 0.0:
+            out.append(verify_chain_greedy(target[b, :g + 1], draft_tokens[b, :g]))
+            continue
+        u = np.concatenate([uniforms[b, :g], uniforms[b, g:g + 1]])
+        tp = 1.0 if top_ps is None else float(top_ps[b])
+        out.append(verify_chain_sampled(target[b, :g + 1], draft[b, :g], draft_tokens[b, :g], u, T,
+                                        int(top_ks[b]), top_p=tp))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # round termination: EOS and the length limit                      [KV4 §5]
 # ---------------------------------------------------------------------------

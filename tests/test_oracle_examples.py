@@ -350,3 +350,33 @@ def test_sampled_round_with_top_p_keeps_losslessness():
                                            top_p=tp)
                 out[r.tokens[0]] += q[d] / grid.size ** 2
     assert np.abs(out - p).max() < 1e-2
+
+
+# --- per-request gamma / temperature / top-k / top-p (batch layout reading) ----------
+def test_batch_with_per_request_settings_equals_single_requests():
+    """Each request of a padded batch gives exactly the single-request result
+    on its own slice; a request with gamma_b < gamma_max draws its bonus from
+    target row gamma_b with uniform u[gamma_b]."""
+    rng = np.random.default_rng(21)
+    B, gmax, V = 6, 4, 12
+    tgt = rng.normal(0, 2, (B, gmax + 1, V))
+    drf = tgt[:, :gmax] + rng.normal(0, 0.5, (B, gmax, V))
+    tok = rng.integers(0, V, (B, gmax))
+    u = rng.random((B, gmax + 1))
+    gammas = [4, 0, 2, 3, 1, 4]
+    temps = [1.0, 0.7, 0.0, 1.3, 1.0, 0.5]
+    ks = [0, 3, 0, 5, 0, 4]
+    ps = [1.0, 1.0, 1.0, 0.8, 0.5, 0.9]
+    res = O.verify_chain_batch(tgt, drf, tok, u, gammas, temps, ks, ps)
+    for b in range(B):
+        g = gammas[b]
+        if temps[b] == 0.0:
+            want = O.verify_chain_greedy(tgt[b, :g + 1], tok[b, :g])
+        else:
+            want = O.verify_chain_sampled(tgt[b, :g + 1], drf[b, :g], tok[b, :g],
+                                          np.r_[u[b, :g], u[b, g]], temps[b], ks[b], top_p=ps[b])
+        assert res[b].tokens == want.tokens and res[b].n_acc == want.n_acc
+        assert 1 <= res[b].n_out <= g + 1
+    # gamma 0: only the bonus draw, from target row 0 with u[0]
+    p0 = O.transform_probs(tgt[1, 0], 0.7, 3)
+    assert p0[res[1].tokens[0]] > 0 and res[1].n_acc == 0
