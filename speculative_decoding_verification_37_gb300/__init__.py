@@ -9,4 +9,4 @@ from ._lib import (EXPORTED, SPEC_DTYPE_BF16, SPEC_DTYPE_F32, SPEC_ERR_CUDA,  # 
                    spec_get_status, spec_ngram_draft, spec_tree_level, spec_verify_chain,
                    spec_verify_tree, spec_workspace_bytes)
 from .api import (ChainOut, NgramOut, TreeBuilder, TreeOut, chain_workspace_kind,  # noqa: F401
-                  commit_kv, ngram_draft, verify_chain, verify_tree, workspace)
+                  clear_workspaces, commit_kv, ngram_draft, verify_chain, verify_tree, workspace)

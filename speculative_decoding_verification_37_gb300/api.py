@@ -15,7 +15,8 @@ _WORKSPACES: Dict[Tuple, torch.Tensor] = {}
 def workspace(kind: int, B: int, n: int, V: int, device) -> torch.Tensor:
     """A cached zero-filled workspace for (device, kind, B, n, V) (the size of
     some kinds depends on V).  Every call leaves it zeroed, so it is reused
-    without clearing; calls that share it must be ordered on one stream."""
+    without clearing; calls that share it must be ordered on one stream.
+    The cache lives as long as the process; clear_workspaces() frees it."""
     dev = torch.device(device)
     if dev.type == "cuda" and dev.index is None:
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -25,6 +26,13 @@ def workspace(kind: int, B: int, n: int, V: int, device) -> torch.Tensor:
         ws = L.new_workspace(kind, B, n, V, device=dev)
         _WORKSPACES[key] = ws
     return ws
+
+
+def clear_workspaces() -> None:
+    """Drops every cached workspace (after the work using them has finished),
+    e.g. after a timeout (SPEC_FLAG_TIMEOUT asks for a fresh workspace) or
+    when batch shapes change for good."""
+    _WORKSPACES.clear()
 
 
 @dataclass
