@@ -210,3 +210,12 @@ def test_top_p_needs_the_top_k_path(lib):
         ws = ctypes.create_string_buffer(n + 256)
         base = (ctypes.addressof(ws) + 255) // 256 * 256
         assert lib.spec_verify_chain(ctypes.byref(a), ctypes.c_void_p(base), n, None) == L.SPEC_ERR_UNSUPPORTED
+
+
+def test_workspace_cache_and_clear(lib):
+    from speculative_decoding_verification_37_gb300 import api
+    w = api.workspace(L.SPEC_WS_COMMIT, 4, 0, 0, "cpu")
+    assert api.workspace(L.SPEC_WS_COMMIT, 4, 0, 0, "cpu") is w
+    assert int(w.sum()) == 0 and w.numel() >= L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 4, 0, 0)
+    api.clear_workspaces()
+    assert api.workspace(L.SPEC_WS_COMMIT, 4, 0, 0, "cpu") is not w
