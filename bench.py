@@ -346,15 +346,17 @@ def kv_bytes(wl: Workload, n_slots_total: int) -> int:
 # CPU oracle (bounded sample)
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: int, seconds: float = 12.0, seed: int = 0, n_gen: int = 16,
-                  wall_cap: float = 60.0):
+                  wall_cap: float = 60.0, first: int = 0, start=None):
     """Times the fp64 oracle (verify + commit of each request) on this host,
-    one request at a time: the inputs of the workload's first `n_gen` requests
-    are generated once, then the oracle cycles over them until it has run for
-    about `seconds` (or the wall clock reaches `wall_cap`).  Returns
-    (rows/s, sample text, requests run)."""
+    one request at a time: the inputs of `n_gen` requests of the workload
+    (from request `first` on, wrapping around the batch) are generated once,
+    then the oracle cycles over them until it has run for about `seconds` (or
+    the wall clock reaches `wall_cap`).  `start` (a barrier) is waited on
+    after the generation, so that parallel workers time the same interval.
+    Returns (rows/s, sample text, requests run)."""
     import oracle as O
     spec = W.WORKLOADS[cfg]
-    reqs = list(range(min(spec.B, n_gen)))
+    reqs = sorted({(first + i) % spec.B for i in range(min(spec.B, n_gen))})
     if isinstance(spec, W.TreeSpec):
         tb = W.make_tree(spec, seed=seed, requests=reqs)
         kvb = W.make_kv(spec.kv, len(reqs), spec.n_nodes + 1, seed=seed)
@@ -372,11 +374,13 @@ def oracle_sample(cfg: int, seconds: float = 12.0, seed: int = 0, n_gen: int = 1
         temp = kvb.temp_kv.view(torch.int16).numpy()
     rows_done = n_req = passes = 0
     elapsed = 0.0
+    if start is not None:
+        start.wait()
     wall0 = time.perf_counter()
     while elapsed < seconds and time.perf_counter() - wall0 < wall_cap:
         cache = cache0.copy() if kvb is not None else None  # every pass commits into a fresh cache
         t0 = time.perf_counter()
-        for i in range(len(reqs)):
+        for i in range(len(reqs)):  # i indexes the generated (compacted) batch
             if isinstance(spec, W.TreeSpec):
                 r = O.verify_tree(tb.logits_f64(i), tb.node_token[i], tb.node_parent[i],
                                   tb.row_of_node[i], int(kvb.committed_len[i]))
@@ -400,10 +404,77 @@ def oracle_sample(cfg: int, seconds: float = 12.0, seed: int = 0, n_gen: int = 1
                 break
         elapsed += time.perf_counter() - t0
         passes += 1
-    sample = (f"{n_req} request verifications + KV commits over the first {len(reqs)} requests of "
+    sample = (f"{n_req} request verifications + KV commits over {len(reqs)} requests of "
               f"this workload ({passes} passes), {elapsed:.1f} s of oracle time on one core "
               f"(input generation excluded)")
     return rows_done / elapsed, sample, n_req
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(q, start, cfg, seconds, first, n_gen):
+    try:
+        v, _, n = oracle_sample(cfg, seconds=seconds, n_gen=n_gen, first=first, start=start)
+        q.put((v, n, None))
+    except BaseException as e:  # reported by the parent
+        start.abort()
+        q.put((0.0, 0, repr(e)))
+
+
+def oracle_parallel(cfg: int, workers: int, seconds: float, n_gen: int = 4):
+    """The oracle on `workers` processes at once (spawned, one thread each),
+    each over its own requests of the workload, all timed over the same
+    interval after their inputs are generated.  Returns (rows/s summed over
+    the workers, sample text, requests run)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")  # never fork a process that may hold a CUDA context
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        q = ctx.Queue()
+        start = ctx.Barrier(workers)
+        procs = [ctx.Process(target=_oracle_worker, args=(q, start, cfg, seconds, w * n_gen, n_gen))
+                 for w in range(workers)]
+        for p in procs:
+            p.start()
+        res = [q.get(timeout=seconds + 600) for _ in procs]
+        for p in procs:
+            p.join(timeout=60)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    errs = [e for _, _, e in res if e]
+    if errs:
+        raise RuntimeError(f"oracle worker failed: {errs[0]}")
+    total = sum(v for v, _, _ in res)
+    n_req = sum(n for _, n, _ in res)
+    sample = (f"{n_req} request verifications + KV commits on {workers} processes at once (one thread "
+              f"each, {n_gen} requests of this workload per process), about {seconds:.0f} s each, "
+              f"rows/s summed over the processes (input generation excluded)")
+    return total, sample, n_req
+
+
+def cpu_baseline_record(cfg: int, seconds: float = 10.0):
+    """The oracle timed on this host's cores: single-threaded, then one
+    process per core.  `value` and `cores` are the all-cores run's."""
+    cores = host_cores()
+    v1, s1, _ = oracle_sample(cfg, seconds=seconds)
+    if cores > 1:
+        vn, sn, _ = oracle_parallel(cfg, cores, seconds)
+    else:
+        vn, sn = v1, s1
+    return {"value": vn, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sn,
+            "host_cores": os.cpu_count(), "single_core": {"value": v1, "cores": 1, "sample": s1}}
 
 
 # ---------------------------------------------------------------------------
@@ -456,14 +527,19 @@ def config_dict(cfg: int, world: int, batch: int = 0):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    v, sample, _ = oracle_sample(args.config, seconds=max(2.0, 4.0 * args.steps))
+    cores = host_cores()
+    seconds = min(60.0, max(2.0, 4.0 * args.steps))
+    if cores > 1:
+        v, sample, _ = oracle_parallel(args.config, cores, seconds)
+    else:
+        v, sample, _ = oracle_sample(args.config, seconds=seconds)
     s = W.WORKLOADS[args.config]
     dtype = s.dtype
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic", "config": config_dict(args.config, world),
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -862,8 +938,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, sample, _ = oracle_sample(args.config, seconds=12.0)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+        cpu = cpu_baseline_record(args.config)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

@@ -319,9 +319,16 @@ int spec_commit_kv(const SpecCommitArgs *args, void *workspace, size_t workspace
  *     order them on one stream.
  *   * A call needing more scratch than the array holds (see
  *     spec_workspace_bytes(SPEC_WS_CHAIN, B, gamma, V)) returns
- *     SPEC_ERR_TOO_LARGE before enqueuing anything.  1 MiB covers, e.g.,
+ *     SPEC_ERR_TOO_LARGE.  1 MiB covers, e.g.,
  *     B = 4096 requests at gamma = 8.
  *   * There is no status word to read back: data errors show in flags[b].
+ *   * The array holds the plain chain workspace only, without the top-k
+ *     path's candidate regions or the full-vocabulary path's state: top-k
+ *     calls take the cluster kernel's exact threshold search (same results,
+ *     slower), full-vocabulary calls the cluster kernel, and a sampled call
+ *     with 0 < top_p < 1 returns SPEC_ERR_UNSUPPORTED.
+ *   * Every argument check (including SPEC_ERR_TOO_LARGE and the top-p case)
+ *     returns before anything is enqueued.
  */
 #define SPEC_STATIC_WORKSPACE_BYTES (1u << 20)
 int spec_verify_chain_static(const SpecChainArgs *args, void *stream);

@@ -219,14 +219,18 @@ extern "C" size_t spec_workspace_bytes(int kind, int32_t B, int32_t n, int32_t V
     }
 }
 
-extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t ws_bytes,
-                                 void *stream) {
+namespace specv {
+
+// Every host-side check of a chain call's arguments except the workspace's:
+// SPEC_OK or the code the call returns, before anything is enqueued.
+int chain_args_check(const SpecChainArgs *a) {
     if (!a) return SPEC_ERR_INVALID_ARG;
     if (a->B < 0 || a->gamma < 0 || a->gamma > 4096 || a->V < 1) return SPEC_ERR_INVALID_ARG;
     if (a->dtype != SPEC_DTYPE_BF16 && a->dtype != SPEC_DTYPE_F32) return SPEC_ERR_INVALID_ARG;
     if (!(a->temperature >= 0.0f) || !std::isfinite(a->temperature)) return SPEC_ERR_INVALID_ARG;
     if (a->top_k < 0 || !(a->fallback_eps >= 0.0f) || !std::isfinite(a->fallback_eps))
         return SPEC_ERR_INVALID_ARG;
+    if (!(a->top_p >= 0.0f) || !std::isfinite(a->top_p)) return SPEC_ERR_INVALID_ARG;
     if (a->B == 0) return SPEC_OK;
     const bool greedy = a->temperature == 0.0f;
     if (!a->target_logits || a->target_row_stride < a->V) return SPEC_ERR_INVALID_ARG;
@@ -235,6 +239,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     if (!greedy) {
         if (!a->uniforms) return SPEC_ERR_INVALID_ARG;
         if (a->gamma > 0 && (!a->draft_logits || a->draft_row_stride < a->V)) return SPEC_ERR_INVALID_ARG;
+        if (!std::isfinite((float)(1.4426950408889634074 / (double)a->temperature))) return SPEC_ERR_INVALID_ARG;
     }
     const size_t es = esize(a->dtype);
     if (!aligned(a->target_logits, es) || (a->draft_logits && !aligned(a->draft_logits, es)))
@@ -242,10 +247,21 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     if (a->blocks_in_use && (!a->committed_len || a->block_size < 1)) return SPEC_ERR_INVALID_ARG;
     if (a->draft_len && !a->committed_len) return SPEC_ERR_INVALID_ARG;
     if (a->kv_capacity < 0) return SPEC_ERR_INVALID_ARG;
-    InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
     if (a->eos_enabled && (a->eos_token < 0 || a->eos_token >= a->V)) return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
+
+}  // namespace specv
+
+extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+    const int chk = chain_args_check(a);
+    if (chk != SPEC_OK) return chk;
+    if (a->B == 0) return SPEC_OK;
+    const bool greedy = a->temperature == 0.0f;
+    const size_t es = esize(a->dtype);
+    InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
     const StopRule stop{a->eos_enabled ? a->eos_token : -1, a->max_new};
-    if (!(a->top_p >= 0.0f) || !std::isfinite(a->top_p)) return SPEC_ERR_INVALID_ARG;
     const bool nucleus = a->top_p > 0.0f && a->top_p < 1.0f && !greedy;
     const int64_t rows = (int64_t)a->B * (a->gamma + 1);
     if (!workspace || !aligned(workspace, 256) ||

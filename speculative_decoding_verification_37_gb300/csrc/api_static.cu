@@ -37,10 +37,16 @@ std::once_flag g_ws_once[kMaxDevices];
 }  // namespace
 
 extern "C" int spec_verify_chain_static(const SpecChainArgs *a, void *stream) {
-    if (!a || a->B < 0 || a->gamma < 0) return SPEC_ERR_INVALID_ARG;
+    // every host-side check comes before the memset below, so a rejected
+    // call enqueues nothing
+    const int chk = specv::chain_args_check(a);
+    if (chk != SPEC_OK) return chk;
+    if (a->B == 0) return SPEC_OK;
     const size_t need = spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V);
     if (need > kStaticWsBytes) return SPEC_ERR_TOO_LARGE;
-    if (a->B == 0) return spec_verify_chain(a, nullptr, 0, stream);  // validates, launches nothing
+    // top-p is cut from the top-k path's candidate regions, which this
+    // array does not hold
+    if (a->temperature > 0.0f && a->top_p > 0.0f && a->top_p < 1.0f) return SPEC_ERR_UNSUPPORTED;
 
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);

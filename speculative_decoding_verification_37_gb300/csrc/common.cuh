@@ -274,8 +274,6 @@ __device__ __forceinline__ void inplace_commit(const IP &ip, int b, int len0, in
     if (ip.blocks_in_use) ip.blocks_in_use[b] = (int)(((int64_t)nl + ip.block_size - 1) / ip.block_size);
 }
 
-// Sets a kernel's dynamic shared-memory limit once per device (the setting
-// is per device; doing it once keeps it out of captured launch sequences).
 // Early end of a chain round ("KV Cache 优化（四）" §5): the emitted tokens
 // are cut right after the first end-of-sequence token, then to the request's
 // remaining length.  stop_limit: the limit of request b (INT_MAX if none);
@@ -302,12 +300,17 @@ __device__ __forceinline__ int stop_length(int n, int cut, int lim, unsigned &fl
     return L;
 }
 
+// Sets a kernel's dynamic shared-memory limit once per device (the setting
+// is per device; doing it once keeps it out of captured launch sequences).
+// Devices 0..63 remember that it is done; a higher device id sets it on
+// every call.
 template <typename K>
 inline cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<unsigned long long> &done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
+    if (dev < 0 || dev >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const unsigned long long bit = 1ull << dev;
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);

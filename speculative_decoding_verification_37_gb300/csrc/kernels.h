@@ -6,7 +6,13 @@
 
 #include "ddmath.cuh"
 
+struct SpecChainArgs;
+
 namespace specv {
+
+// Host-side checks of a chain call's arguments (all but the workspace):
+// SPEC_OK or the error code the call returns before enqueuing anything.
+int chain_args_check(const SpecChainArgs *a);
 
 // Workspace layout shared by every verify kind: a sticky status word, one
 // arrival counter per request, then per-row argmax keys or per-position

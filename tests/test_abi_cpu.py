@@ -119,6 +119,23 @@ def test_chain_host_validation(lib, bad):
     assert lib.spec_verify_chain(ctypes.byref(a), ws, 1 << 16, None) == L.SPEC_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("bad", [
+    dict(V=0), dict(dtype=7), dict(temperature=float("nan")), dict(top_k=-2),
+    dict(target_logits=None), dict(uniforms=None), dict(draft_row_stride=3),
+    dict(eos_enabled=1, eos_token=16), dict(top_p=float("nan")),
+])
+def test_static_entry_point_checks_arguments_first(lib, bad):
+    """spec_verify_chain_static refuses every bad call before it touches
+    CUDA: on this GPU-less host any CUDA call (the device lookup, the memset
+    of its array) would fail with SPEC_ERR_CUDA instead."""
+    a = _chain_args(**bad)
+    assert lib.spec_verify_chain_static(ctypes.byref(a), None) == L.SPEC_ERR_INVALID_ARG
+    # top-p needs the candidate regions the fixed array does not hold
+    a = _chain_args(top_p=0.9, top_k=5)
+    assert lib.spec_verify_chain_static(ctypes.byref(a), None) == L.SPEC_ERR_UNSUPPORTED
+    assert lib.spec_verify_chain_static(ctypes.byref(_chain_args(B=0)), None) == L.SPEC_OK
+
+
 def test_chain_workspace_validation(lib):
     a = _chain_args()
     assert lib.spec_verify_chain(ctypes.byref(a), None, 0, None) == L.SPEC_ERR_INVALID_ARG

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle as O
-from parity import compare_chain, run_chain
+from parity import compare_chain, full_path_used, run_chain
 from speculative_decoding_verification_37_gb300 import _lib as L
 from speculative_decoding_verification_37_gb300 import api
 from speculative_decoding_verification_37_gb300 import workloads as W
@@ -26,16 +26,6 @@ pytestmark = pytest.mark.gpu
 def spec(B, gamma, V, dtype, T, draft_sigma=1.0, sigma=2.0):
     return W.ChainSpec(f"t B={B} g={gamma} V={V}", B=B, gamma=gamma, V=V, dtype=dtype,
                        target_sigma=sigma, temperature=T, top_k=0, draft_sigma=draft_sigma)
-
-
-def full_path_used(B, gamma, V):
-    """The full path writes its per-slice statistics right after the plain
-    chain workspace; the other kernels never touch that region."""
-    torch.cuda.synchronize()
-    ws = api.workspace(L.SPEC_WS_CHAIN_FULL, B, gamma, V, "cuda")
-    plain = L.spec_workspace_bytes(L.SPEC_WS_CHAIN, B, gamma, V)
-    plain = (plain + 255) // 256 * 256
-    return bool(ws[plain:plain + 256].any())
 
 
 def run_full(batch):

@@ -1,7 +1,12 @@
-"""GPU parity at the five workloads' full sizes, in the launch configuration
-the benchmark times: every request is checked against the oracle; the KV
-commit is checked block by block on the blocks it may touch, and every other
-block must still hold the sentinel."""
+"""GPU parity at the five workloads' full sizes: every request is checked
+against the oracle; the KV commit is checked block by block on the blocks it
+may touch, and every other block must still hold the sentinel.
+
+Each workload runs in the launch configuration the benchmark times (the
+same workspace kind, hence the same kernels).  Asking for residual_mass
+changes the kernel on the full-vocabulary workload (the persistent path does
+not write it), so workload 5 runs twice: once as the benchmark runs it, once
+with the residual mass so that output is checked too."""
 import dataclasses
 
 import numpy as np
@@ -9,7 +14,8 @@ import pytest
 import torch
 
 import oracle as O
-from parity import BOUNDARY_RATE_MAX, ChainTally, compare_chain, run_chain
+from parity import BOUNDARY_RATE_MAX, ChainTally, compare_chain, full_path_used, run_chain
+from speculative_decoding_verification_37_gb300 import _lib as L
 from speculative_decoding_verification_37_gb300 import api
 from speculative_decoding_verification_37_gb300 import workloads as W
 
@@ -52,11 +58,11 @@ def commit_and_check(kvb: W.KVBatch, n_slots, slots=None):
     np.testing.assert_array_equal(lens.cpu().numpy(), want_len)
 
 
-def check_chain_config(cfg, residual=True):
+def check_chain_config(cfg, residual=True, batch=None, oracle_results=None):
     spec = W.WORKLOADS[cfg]
-    batch = W.make_chain(spec, seed=0)
+    batch = W.make_chain(spec, seed=0) if batch is None else batch
     gpu = run_chain(batch, residual=residual)
-    tally = compare_chain(batch, gpu, range(batch.n))
+    tally = compare_chain(batch, gpu, range(batch.n), oracle_results=oracle_results)
     assert tally.boundary <= 1, tally.boundary
     return batch, gpu, tally
 
@@ -105,13 +111,24 @@ def test_config4_tree_and_commit():
 
 
 def test_config5_chain_f32_equal_rows_and_commit():
-    batch, gpu, t = check_chain_config(5)
+    """Workload 5 (B=512, gamma=7, V=128256 fp32, 5 requests with draft ==
+    target): first on the persistent full-vocabulary kernel, routed exactly as
+    the benchmark routes it (SPEC_WS_CHAIN_FULL workspace, no residual_mass),
+    then on the cluster kernel that also writes residual_mass; one oracle run
+    serves both comparisons."""
+    spec = W.WORKLOADS[5]
+    batch = W.make_chain(spec, seed=0)
+    assert api.chain_workspace_kind(True, spec.top_k, spec.V) == L.SPEC_WS_CHAIN_FULL
+    results = {}
+    _, gpu_full, t_full = check_chain_config(5, residual=False, batch=batch, oracle_results=results)
+    assert full_path_used(spec.B, spec.gamma, spec.V)
+    assert gpu_full["residual_mass"] is None and t_full.requests == spec.B
+    _, gpu, t = check_chain_config(5, residual=True, batch=batch, oracle_results=results)
     for b in batch.equal_rows:
-        assert gpu["n_acc"][b] == batch.spec.gamma
+        assert gpu_full["n_acc"][b] == spec.gamma and gpu["n_acc"][b] == spec.gamma
         assert np.all(gpu["residual_mass"][b] == 0.0)
-    spec = batch.spec
     kvb = W.make_kv(spec.kv, spec.B, spec.gamma + 1, seed=0)
-    commit_and_check(kvb, gpu["n_out"])
+    commit_and_check(kvb, gpu_full["n_out"])
 
 
 def test_boundary_case_rate_on_many_decisions():

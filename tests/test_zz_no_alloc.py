@@ -59,10 +59,16 @@ def test_static_scratch_matches_workspace_entry_point_twice(name):
     ref = _outputs(B, g, sampled, dev)
     ws = api.workspace(L.SPEC_WS_CHAIN, B, g, spec.V, dev)
     L.spec_verify_chain(workspace=ws, **common, **ref)
+    outs = [_outputs(B, g, sampled, dev) for _ in range(2)]
+    torch.cuda.synchronize()
+    # the device's free memory is read with every buffer of the test already
+    # allocated: the static calls must not change it
+    free0 = torch.cuda.mem_get_info()[0]
     for call in range(2):
-        got = _outputs(B, g, sampled, dev)
+        got = outs[call]
         L.spec_verify_chain_static(**common, **got)
         torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0, call
         for key in ("n_acc", "n_out", "out_tokens", "flags"):
             assert torch.equal(got[key], ref[key]), (call, key)
         if sampled:
@@ -83,3 +89,22 @@ def test_static_scratch_rejects_oversized_batches():
     assert L.lib().spec_verify_chain_static(ctypes.byref(a), None) == L.SPEC_ERR_TOO_LARGE
     assert b"static workspace" in L.lib().spec_error_string(L.SPEC_ERR_TOO_LARGE)
     assert np.isfinite(need)
+
+
+def test_static_scratch_refuses_top_p_before_enqueuing():
+    """Top-p is cut from the top-k path's candidate regions, which the fixed
+    array does not hold: such a call is refused up front."""
+    _build.build()
+    spec = CASES["topk"]
+    dev = "cuda"
+    batch = W.make_chain(spec, seed=3)
+    got = _outputs(spec.B, spec.gamma, True, dev)
+    with pytest.raises(RuntimeError, match="unsupported"):
+        L.spec_verify_chain_static(target_logits=batch.target.to(dev),
+                                   draft_tokens=torch.from_numpy(batch.draft_tokens).to(dev),
+                                   gamma=spec.gamma, temperature=spec.temperature,
+                                   draft_logits=batch.draft.to(dev),
+                                   uniforms=torch.from_numpy(batch.uniforms).to(dev),
+                                   top_k=spec.top_k, top_p=0.9, **got)
+    torch.cuda.synchronize()
+    assert int(got["n_out"].min()) == -7  # nothing ran
