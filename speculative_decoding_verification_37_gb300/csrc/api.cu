@@ -55,8 +55,9 @@ struct Ws {
     unsigned *counters;  // [B] arrival counters
     unsigned *rejword;   // [B] earliest rejection per request (chain, sampled)
     void *data;          // chain: records or argmax keys; tree: argmax keys
-    uint2 *slicecb;      // chain, top-k: [B*(gamma+1)][2][cmax] (count, bound key)
-    uint2 *pool;         // chain, top-k: [B*(gamma+1)][2][cmax][kTopKSlicePool]
+    TopkRow *rkrow;      // chain, top-k: [B*(gamma+1)][2] published kept-set headers
+    uint2 *rkent;        // chain, top-k: [B*(gamma+1)][2][kKeptRowMax] kept entries
+    unsigned *rkcnt;     // chain, top-k: [B*(gamma+1)] position arrival counters (zeroed)
     // chain, full vocabulary: see SampleParams
     float2 *fpart, *fxd;
     float4 *fstat;
@@ -66,12 +67,6 @@ struct Ws {
     DrawPart *dpart;
     int *amb;
 };
-
-// One layout for sizing and for pointers.  `rows` = B*(gamma+1) for a chain
-// (0 for other kinds), `data_bytes` the per-row keys or records.
-// Slices per row of the top-k path; the workspace is sized for the larger
-// count (fp32 rows), so one size serves both element types.
-int topk_slices(int V, int dtype) { return slices_for(V, dtype, 1 << 20, topk_row_bytes()); }
 
 // Slices per row of the full-vocabulary path (sized for fp32 rows, so one
 // size serves both element types).
@@ -105,12 +100,13 @@ size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_
         return at;
     };
     if (extra == kWsPool) {
-        const size_t cmax = (size_t)topk_slices(V, SPEC_DTYPE_F32);
-        char *cb = take(rows * 2 * cmax * sizeof(uint2));
-        char *pl = take(rows * 2 * cmax * (size_t)kTopKSlicePool * sizeof(uint2));
+        char *rc = take(rows * sizeof(unsigned));
+        char *rh = take(rows * 2 * sizeof(TopkRow));
+        char *re = take(rows * 2 * (size_t)kKeptRowMax * sizeof(uint2));
         if (w) {
-            w->slicecb = reinterpret_cast<uint2 *>(cb);
-            w->pool = reinterpret_cast<uint2 *>(pl);
+            w->rkcnt = reinterpret_cast<unsigned *>(rc);
+            w->rkrow = reinterpret_cast<TopkRow *>(rh);
+            w->rkent = reinterpret_cast<uint2 *>(re);
         }
     } else if (extra == kWsFull) {
         const size_t c = (size_t)full_slices(V, SPEC_DTYPE_F32), nb = (size_t)B;
@@ -330,8 +326,9 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.counters = w.counters;
         p.rejword = w.rejword;
         p.recs = static_cast<PosRec *>(w.data);
-        p.slicecb = w.slicecb;
-        p.pool = w.pool;
+        p.rkrow = w.rkrow;
+        p.rkent = w.rkent;
+        p.rkcnt = w.rkcnt;
         p.fpart = w.fpart;
         p.fxd = w.fxd;
         p.fstat = w.fstat;
@@ -365,17 +362,12 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
             e = launch_chain_full(p, a->dtype, sm_count(), s);
             return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
         }
-        // top-k <= 128: cluster-free candidate lists when every slice's share
-        // (about k + a few) fits the per-position pool; otherwise the cluster
-        // kernel with its exact threshold search
-        const int cf = topk_slices(a->V, a->dtype);
-        const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax &&
-                          (int64_t)cf * (p.top_k + 16) <= kTopKMerge;
-        if (nucleus && !fast) return SPEC_ERR_UNSUPPORTED;  // the nucleus is built in the top-k merge
+        // top-k <= 128: one block per row, kept sets published per position;
+        // otherwise the cluster kernel with its exact threshold search
+        const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax;
+        if (nucleus && !fast) return SPEC_ERR_UNSUPPORTED;  // the nucleus is cut from the row kernel's kept set
         if (fast) {
-            p.c = cf;
-            p.Vs = slice_len(a->V, cf);
-            if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+            if ((int64_t)a->B * (2 * (int64_t)a->gamma + 1) > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
             e = launch_chain_topk(p, a->dtype, sm_count(), s);
         } else {
             if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;

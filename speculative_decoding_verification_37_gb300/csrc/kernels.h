@@ -65,7 +65,19 @@ struct ArgmaxParams {
     StopRule stop;
 };
 
-constexpr int kTopKFastMax = 128;  // top_k served by the candidate-list path
+constexpr int kTopKFastMax = 128;  // top_k served by the row-per-block path
+constexpr int kKeptRowMax = 256;   // kept entries of one row the top-k path publishes
+
+// One row's kept set on the top-k path, published for its position's
+// deciding block (16-byte words, read with two vector loads).
+struct alignas(16) TopkRow {
+    unsigned kn;      // kept entries, token order, in the row's entry array
+    unsigned th;      // order key of the threshold: every kept logit's key is >= it
+    float m;          // largest kept logit (-inf: no finite logit)
+    float s_hi, s_lo; // sum over the kept set of exp((l - m)/T), double-float
+    unsigned flags;   // 1: the kept set did not fit (the position takes the exact path)
+    unsigned pad[2];
+};
 
 // Full-vocabulary persistent path (verify_full.cu): a request's draw record
 // and one (request, slice) result of a draw round.
@@ -99,11 +111,11 @@ struct SampleParams {
     unsigned *status, *counters;
     unsigned *rejword;  // [B] earliest rejection seen: gamma - k + 1, 0 = none
     PosRec *recs;       // [B*(gamma+1)]
-    // top-k path: per (position, row, slice) the candidate count with the
-    // bound's order key, and a region of kTopKSlicePool (order key, token id)
-    // entries, slice stride c
-    uint2 *slicecb;      // [B*(gamma+1)][2][c]
-    uint2 *pool;         // [B*(gamma+1)][2][c][kTopKSlicePool]
+    // top-k path: per (position, row) the kept set published for the
+    // position's deciding block, and one arrival counter per position
+    TopkRow *rkrow;      // [B*(gamma+1)][2]
+    uint2 *rkent;        // [B*(gamma+1)][2][kKeptRowMax] (order key, token id), token order
+    unsigned *rkcnt;     // [B*(gamma+1)], zero between calls
     // full-vocabulary persistent path, c = slices of full_row_bytes()
     float2 *fpart;               // [B*(gamma+1)][2][c] (max, sum) per slice
     float2 *fxd;                 // [B*(gamma+1)] target and draft logit at the draft token
@@ -120,8 +132,6 @@ struct SampleParams {
     StopRule stop;
 };
 
-constexpr int kTopKSlicePool = 256;  // candidates one slice of one row may hand on
-constexpr int kTopKMerge = 4096;     // candidates per row one position can merge
 
 struct CommitParams {
     int B, L, S, bs, unit_bytes, max_blocks, slots_stride;

@@ -25,7 +25,7 @@ constexpr int kNW = kNT / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kSeg = 256;        // candidates one top-k slice may contribute per row
 constexpr int kScanE = 8;        // elements per thread per tile of the token-order scan
-constexpr int kKeptMax = 256;    // kept (top-k) entries per row a position can sort
+constexpr int kKeptMax = kKeptRowMax;  // kept (top-k) entries per row a position can sort
 constexpr int kAmbMax = 128;     // residual elements per CTA left to the exact sums (more: a full pass)
 // Margin of the residual classification: p_i > q_i is decided from the fp32
 // estimate of S_p/S_q (relative error below ~2e-5) only outside this band.
@@ -50,11 +50,7 @@ struct SampBase {
     int namb;                     // ambiguous residual elements listed by this CTA
     int amb[kAmbMax];             // their indices
     unsigned rej;                 // earliest-rejection word, pushed by rank 0
-    unsigned ovf;                 // candidate-list overflow, OR-ed by every rank
-    int found, lastpos, arrive_last;
-    unsigned hist[256];
-    unsigned bc[2];
-    unsigned tau[2];
+    int found, lastpos;
     DdExpTables K;                // the double-float exponential's constants
 };
 
@@ -147,8 +143,8 @@ __device__ __forceinline__ void for_slice2(const T *ra, const T *rb, int lo, int
 // ring.  f(xa[VEC], xb[VEC], base, cnt) as in for_slice2.  Rows whose 16-byte
 // phases differ take the register path instead.  Returns false on a wait
 // timeout.
-template <typename T, typename F>
-__device__ bool stream_rows(SampRing &R, const T *trow, const T *drow, int lo, int hi, F &&f) {
+template <typename T, int CH, int NST, typename F>
+__device__ bool stream_rows(Ring<CH, NST, 2> &R, const T *trow, const T *drow, int lo, int hi, F &&f) {
     constexpr int VEC = Elem<T>::VEC;
     const int tid = threadIdx.x;
     const SliceSplit sp = split_slice(trow, lo, hi);
@@ -421,7 +417,7 @@ struct SoloEx {
 // runs it on its slice [lo, hi); the CTA that ends up holding the whole
 // outcome calls finish().
 // ---------------------------------------------------------------------------
-template <typename T, bool MASK, typename Ex>
+template <typename T, bool MASK, typename Ex, typename RingT = SampRing>
 __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned char *dsm, Ex &ex,
                                 int k, int b, int lo, int hi) {
     constexpr int VEC = Elem<T>::VEC;
@@ -481,7 +477,7 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     // ---- pass 1 (HBM): online max / sum of the kept logits -------------------
     MaxSum msp{-INFINITY, 0.0f}, msq{-INFINITY, 0.0f};
     {
-        SampRing &R = *reinterpret_cast<SampRing *>(dsm);
+        RingT &R = *reinterpret_cast<RingT *>(dsm);
         const bool okc = stream_rows<T>(R, trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
             ms_update<VEC, MASK>(msp, xa, cnt, th_p, KS, c2);
             if (has_draft) ms_update<VEC, MASK>(msq, xb, cnt, th_q, KS, c2);
