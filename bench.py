@@ -15,6 +15,11 @@ HBM when a step starts and L2 is flushed (a 256 MiB write) between steps.
 bounded sample of the same workload.  Under torchrun every rank runs its own
 batch (weak scaling, no collective on the data path); the slowest rank's
 time is used.
+
+A single-GPU default run also times, each on its own workload and outside
+the headline value, every other kernel with a bandwidth target (the greedy,
+tree and full-vocabulary verify calls with their KV commits, the draft-tree
+builder, the n-gram drafter) and reports them under "extra".
 """
 from __future__ import annotations
 
@@ -342,6 +347,60 @@ def kv_bytes(wl: Workload, n_slots_total: int) -> int:
     return 0 if wl.kvb is None else 2 * wl.kvb.kv.token_bytes * n_slots_total
 
 
+def kernel_name(wl: Workload) -> str:
+    """The kernels one verify call of this workload launches."""
+    from speculative_decoding_verification_37_gb300 import _lib as L
+    if wl.kind == "tree" or wl.spec.greedy:
+        return "argmax_pass_kernel+argmax_decide_kernel"
+    if 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
+        return "chain_topk_row_kernel"
+    if (wl.spec.top_k == 0 or wl.spec.top_k >= wl.spec.V) and \
+            wl.rows * -(-wl.spec.V * wl.spec.esize // 4096) >= 1024:
+        return "chain_full_kernel"  # the persistent full-vocabulary path (at least 1,024 4 KiB items)
+    return "chain_sample_kernel"
+
+
+def time_steps(step: "Step", steps: int, warmup: int, flush):
+    """Warm-up replays, then `steps` timed replays with the L2 flushed before
+    each; returns the per-step (step, verify, commit) times in ms."""
+    for _ in range(warmup):
+        step.reset()
+        step.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        step.reset()
+        flush.zero_()
+        step.replay(events=ev[i])
+    torch.cuda.synchronize()
+    return ([e[0].elapsed_time(e[2]) for e in ev], [e[0].elapsed_time(e[1]) for e in ev],
+            [e[1].elapsed_time(e[2]) for e in ev])
+
+
+def verify_workload_record(cfg: int, dev, steps: int, warmup: int, flush, peak: float) -> dict:
+    """Times workload `cfg`'s verify (+ commit) step on its own and returns
+    the kernels' device times, algorithmic bytes and fractions of the peak."""
+    wl = Workload(cfg, seed=0, device=dev)
+    step = Step(wl)
+    step.capture()
+    step_ms, verify_ms, commit_ms = time_steps(step, steps, warmup, flush)
+    t_v = statistics.mean(verify_ms)
+    rec = {"workload": wl.spec.name, "kernel": kernel_name(wl), "verify_ms": round(t_v, 5),
+           "algorithmic_bytes": wl.logit_bytes,
+           "achieved_gbs": round(wl.logit_bytes / (t_v * 1e-3) / 1e9, 1),
+           "frac": round(wl.logit_bytes / (t_v * 1e-3) / 1e9 / peak, 4),
+           "rows_per_s": wl.rows / (statistics.mean(step_ms) * 1e-3), "steps": steps}
+    if wl.kvb is not None:
+        n_commit = int(step.n_slots.sum().item())
+        t_c = statistics.mean(commit_ms)
+        kvb = kv_bytes(wl, n_commit)
+        rec.update(commit_kernel="commit_kv_kernel", commit_ms=round(t_c, 5), commit_bytes=kvb,
+                   commit_frac=round(kvb / (t_c * 1e-3) / 1e9 / peak, 4), committed_tokens=n_commit)
+    del step, wl
+    torch.cuda.empty_cache()
+    return rec
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (bounded sample)
 # ---------------------------------------------------------------------------
@@ -548,6 +607,40 @@ def run_reference(args, rank, world):
 NGRAM_METRIC = "n-gram drafts: requests/s + history GB/s vs peak"
 
 
+def ngram_times(run, d_hist, d_lens, steps, warmup, flush):
+    """Device times (ms) of `steps` drafter launches, L2 flushed before each."""
+    for _ in range(max(3, warmup)):
+        run(d_hist, d_lens)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run(d_hist, d_lens)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def ngram_record(dev, steps, warmup, flush, peak) -> dict:
+    """The drafter on its workload, timed on its own (for the default line)."""
+    from speculative_decoding_verification_37_gb300 import api
+    spec = W.NGRAM_SPEC
+    hist, lens = W.make_histories(spec, seed=0)
+    hist_bytes = int(lens.astype(np.int64).sum()) * 4
+    d_hist, d_lens = torch.from_numpy(hist).to(dev), torch.from_numpy(lens).to(dev)
+    run = lambda h, l: api.ngram_draft(h, l, gamma=spec.gamma, n_min=spec.n_min, n_max=spec.n_max)
+    t = statistics.mean(ngram_times(run, d_hist, d_lens, steps, warmup, flush))
+    del d_hist, d_lens
+    torch.cuda.empty_cache()
+    return {"workload": spec.name, "kernel": "ngram_draft_kernel", "ms": round(t, 5),
+            "algorithmic_bytes": hist_bytes, "achieved_gbs": round(hist_bytes / (t * 1e-3) / 1e9, 1),
+            "frac": round(hist_bytes / (t * 1e-3) / 1e9 / peak, 4),
+            "requests_per_s": spec.B / (t * 1e-3), "steps": steps}
+
+
 def run_ngram(args, rank, world, local):
     """The prompt-lookup drafter on a batch of long histories (one launch per
     step, histories resident; L2 flushed between steps)."""
@@ -579,21 +672,10 @@ def run_ngram(args, rank, world, local):
     d_lens = torch.from_numpy(lens).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     run = lambda h, l: api.ngram_draft(h, l, gamma=spec.gamma, n_min=spec.n_min, n_max=spec.n_max)
-    for _ in range(max(3, args.warmup)):
-        run(d_hist, d_lens)
-    torch.cuda.synchronize()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     barrier(world)
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        run(d_hist, d_lens)
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
+    times = ngram_times(run, d_hist, d_lens, args.steps, args.warmup, flush)
     barrier(world)
     clk = clocks.stop()
     t = max_over_ranks(statistics.mean(times), world)
@@ -657,6 +739,65 @@ def tree_build_oracle_sample(levels, spec, seconds: float):
                     f"{el:.1f} s on one core")
 
 
+def tree_build_graph(spec, d_levels, dev, warmup):
+    """A TreeBuilder over the levels' draft rows, its three level calls
+    captured in one CUDA graph and warmed up."""
+    from speculative_decoding_verification_37_gb300 import api
+    tb = api.TreeBuilder(spec.B, spec.V, spec.topKSpec, spec.topHead, dev)
+
+    def build_all():
+        for i, lv in enumerate(d_levels):
+            tb.level(lv, i)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            build_all()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        build_all()
+    for _ in range(max(3, warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    return tb, build_all, graph
+
+
+def graph_times(graph, steps, flush):
+    """Device times (ms) of `steps` replays, L2 flushed before each."""
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def tree_build_record(dev, steps, warmup, flush, peak) -> dict:
+    """The draft-tree builder on the tree workload's shape, timed on its own
+    (for the default line)."""
+    spec = W.WORKLOADS[4]
+    levels = W.make_tree_levels(spec, seed=0)
+    logit_bytes = sum(lv.numel() * lv.element_size() for lv in levels)
+    d_levels = [lv.to(dev) for lv in levels]
+    tb, _, graph = tree_build_graph(spec, d_levels, dev, warmup)
+    t = statistics.mean(graph_times(graph, steps, flush))
+    del graph, tb, d_levels
+    torch.cuda.empty_cache()
+    return {"workload": f"tree build {[list(k) for k in spec.topKSpec]}/{list(spec.topHead)} B={spec.B} "
+                        f"V={spec.V} {spec.dtype}",
+            "kernel": "tree_level_kernel+tree_merge_kernel (3 levels)", "ms": round(t, 5),
+            "algorithmic_bytes": logit_bytes, "achieved_gbs": round(logit_bytes / (t * 1e-3) / 1e9, 1),
+            "frac": round(logit_bytes / (t * 1e-3) / 1e9 / peak, 4), "trees_per_s": spec.B / (t * 1e-3),
+            "steps": steps}
+
+
 def run_tree_build(args, rank, world, local):
     """The draft-tree builder over the tree workload's shape: one step is the
     three level calls of a whole tree (captured in one CUDA graph), the draft
@@ -690,25 +831,7 @@ def run_tree_build(args, rank, world, local):
     torch.cuda.set_device(dev)
     d_levels = [lv.to(dev) for lv in levels]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    tb = api.TreeBuilder(spec.B, spec.V, spec.topKSpec, spec.topHead, dev)
-
-    def build_all():
-        for i, lv in enumerate(d_levels):
-            tb.level(lv, i)
-
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        for _ in range(2):
-            build_all()
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        build_all()
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
-    torch.cuda.synchronize()
+    tb, build_all, graph = tree_build_graph(spec, d_levels, dev, args.warmup)
     # per-level launch times (eager, events between the calls)
     lvl_ms = [[] for _ in d_levels]
     for _ in range(3):
@@ -724,15 +847,7 @@ def run_tree_build(args, rank, world, local):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     barrier(world)
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        graph.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
+    times = graph_times(graph, args.steps, flush)
     barrier(world)
     clk = clocks.stop()
     t = max_over_ranks(statistics.mean(times), world)
@@ -812,6 +927,9 @@ def main():
     ap.add_argument("--workload", default="verify", choices=["verify", "ngram", "tree_build"],
                     help="ngram: the prompt-lookup drafter on long token histories; tree_build: "
                          "the draft-tree builder on the tree workload's shape")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads' kernel lines (workloads 3-5, the tree builder, "
+                         "the n-gram drafter) that a single-GPU default run adds under 'extra'")
     ap.add_argument("--kv-commit", default="copy", choices=["copy", "inplace"],
                     help="inplace (chain): K/V written in place by the forward, the verify "
                          "call advances the lengths, no commit kernel")
@@ -849,21 +967,13 @@ def main():
     # timed steps: per-step events around the graph replays; the length reset
     # and the L2 flush (which also keeps the GPU busy while the host enqueues)
     # sit between the events
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        step.reset()
-        flush.zero_()
-        step.replay(events=ev[i])
-    torch.cuda.synchronize()
+    step_ms, verify_ms, commit_ms = time_steps(step, args.steps, 0, flush)
     barrier(world)
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    verify_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    commit_ms = [e[1].elapsed_time(e[2]) for e in ev]
     n_commit_total = int(step.n_slots.sum().item()) if wl.kvb is not None else 0
     t_step = statistics.mean(step_ms)
     t_step_max = max_over_ranks(t_step, world)
@@ -873,16 +983,7 @@ def main():
     peak, peak_kind = measured_peaks()
     t_verify = statistics.mean(verify_ms)
     achieved = wl.logit_bytes / (t_verify * 1e-3) / 1e9
-    if wl.kind == "tree" or wl.spec.greedy:
-        kname = "argmax_pass_kernel+argmax_decide_kernel"
-    elif 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
-        # one spec_verify_chain call launches both; timed together
-        kname = "chain_topk_kernel+chain_topk_merge_kernel"
-    elif (wl.spec.top_k == 0 or wl.spec.top_k >= wl.spec.V) and \
-            wl.rows * -(-wl.spec.V * wl.spec.esize // 4096) >= 1024:
-        kname = "chain_full_kernel"  # the persistent full-vocabulary path (at least 1,024 4 KiB items)
-    else:
-        kname = "chain_sample_kernel"
+    kname = kernel_name(wl)
     tr = traffic_record(kname, config_dict(args.config, world, args.batch)["workload"])
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -936,6 +1037,17 @@ def main():
                "path": "pinned host -> device copies, spec_verify + spec_commit_kv, device -> host "
                        "of n_acc/out_tokens/n_out/committed_len, all in the timed region"}
 
+    # every other kernel with a bandwidth target, each timed on its own
+    # workload (single-GPU default runs only; not part of the headline value)
+    extra = None
+    if world == 1 and not args.no_extra and args.config == 2 and not args.batch and not in_place:
+        x_steps = max(3, min(args.steps, 10))
+        extra = {"note": "each kernel timed alone on its own workload (CUDA graphs, L2 flushed before "
+                         f"each of {x_steps} steps); not part of the headline value",
+                 "workloads": [verify_workload_record(c, dev, x_steps, 3, flush, peak) for c in (3, 4, 5)]}
+        extra["workloads"].append(tree_build_record(dev, x_steps, 3, flush, peak))
+        extra["workloads"].append(ngram_record(dev, x_steps, 3, flush, peak))
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_record(args.config)
@@ -949,7 +1061,7 @@ def main():
                 "rounds_per_s": wl.B * world / (t_step_max * 1e-3),
                 "step_gbs": round((wl.logit_bytes + kv_bytes(wl, n_commit_total)) /
                                   (t_step_max * 1e-3) / 1e9, 1),
-                "roofline": roofline, "commit": commit, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "commit": commit, "cpu_baseline": cpu, "e2e": e2e, "extra": extra,
                 "gpu_launches": args.steps * ((2 if "+" in kname else 1) +
                                               (1 if wl.kvb is not None and not in_place else 0)),
                 "clocks": clk, "kernel_source": kernel_source_hash()}
