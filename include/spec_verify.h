@@ -194,11 +194,32 @@ typedef struct SpecChainArgs {
      * after temperature and top-k each row keeps the smallest set of its
      * most probable tokens whose probability reaches top_p (tokens tied with
      * the least probable kept one are kept too), renormalised; target and
-     * draft alike.  Needs 1 <= top_k <= 128 and a workspace of
-     * SPEC_WS_CHAIN_TOPK size (SPEC_ERR_UNSUPPORTED otherwise).  A position
-     * whose kept set has more than 256 tied logits is flagged
-     * SPEC_FLAG_BAD_ROW.  0 (the zeroed default) or >= 1: off. */
+     * draft alike.  With 1 <= top_k <= 128 and a workspace of
+     * SPEC_WS_CHAIN_TOPK size it is cut from the fast path's kept set;
+     * otherwise the call takes the exact path (below),
+     * where any top_k works, 0 included: the nucleus over the full
+     * vocabulary.  0 (the zeroed default) or >= 1: off. */
     float top_p;
+    /* Per-request settings ("10.6 投机解码" §10.6.3: the requests of one batch
+     * accept different lengths and restart at different points; "KV Cache
+     * 优化（四）" §4: each request's own processed distributions enter its
+     * rule).  Device arrays [B]; NULL = the scalar above for every request.
+     * The row layout stays padded to `gamma`: request b uses target rows
+     * 0..gamma_b, draft rows and draft tokens 0..gamma_b-1, uniforms
+     * u[b][0..gamma_b-1] for its tests and u[b][gamma_b] for its final draw;
+     * out_tokens and accept_prob keep the row stride of `gamma`.  A request
+     * with temperature 0 is greedy (argmax match, lowest index on ties; its
+     * accept_prob entries are 1 or 0 and its residual_mass entries 0).
+     * With any of these arrays given (or top_p set without the top-k fast
+     * path) the call takes the exact path: one thread-block cluster per
+     * position, each request with its own settings; the plain SPEC_WS_CHAIN
+     * workspace suffices.  A value out of range (gamma_b outside [0, gamma],
+     * a temperature that is negative or not finite, top_k < 0, top_p < 0 or
+     * NaN) flags that request SPEC_FLAG_BAD_INPUT. */
+    const int32_t *gamma_per_request;       /* device [B] or NULL */
+    const float *temperature_per_request;   /* device [B] or NULL */
+    const int32_t *top_k_per_request;       /* device [B] or NULL */
+    const float *top_p_per_request;         /* device [B] or NULL */
 } SpecChainArgs;
 
 int spec_verify_chain(const SpecChainArgs *args, void *workspace, size_t workspace_bytes,
@@ -323,12 +344,12 @@ int spec_commit_kv(const SpecCommitArgs *args, void *workspace, size_t workspace
  *     B = 4096 requests at gamma = 8.
  *   * There is no status word to read back: data errors show in flags[b].
  *   * The array holds the plain chain workspace only, without the top-k
- *     path's candidate regions or the full-vocabulary path's state: top-k
- *     calls take the cluster kernel's exact threshold search (same results,
- *     slower), full-vocabulary calls the cluster kernel, and a sampled call
- *     with 0 < top_p < 1 returns SPEC_ERR_UNSUPPORTED.
- *   * Every argument check (including SPEC_ERR_TOO_LARGE and the top-p case)
- *     returns before anything is enqueued.
+ *     path's candidate regions or the full-vocabulary path's state: sampled
+ *     calls take the exact cluster path (top-k by its exact threshold
+ *     search, top-p and per-request settings included; same results,
+ *     slower).
+ *   * Every argument check (SPEC_ERR_TOO_LARGE included) returns before
+ *     anything is enqueued.
  */
 #define SPEC_STATIC_WORKSPACE_BYTES (1u << 20)
 int spec_verify_chain_static(const SpecChainArgs *args, void *stream);

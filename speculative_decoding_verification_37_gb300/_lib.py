@@ -41,7 +41,9 @@ class SpecChainArgs(ctypes.Structure):
                 ("accept_prob", c_void_p), ("residual_mass", c_void_p), ("flags", c_void_p),
                 ("committed_len", c_void_p), ("draft_len", c_void_p), ("blocks_in_use", c_void_p),
                 ("block_size", c_int32), ("kv_capacity", c_int64), ("eos_enabled", c_int32),
-                ("eos_token", c_int32), ("max_new", c_void_p), ("top_p", c_float)]
+                ("eos_token", c_int32), ("max_new", c_void_p), ("top_p", c_float),
+                ("gamma_per_request", c_void_p), ("temperature_per_request", c_void_p),
+                ("top_k_per_request", c_void_p), ("top_p_per_request", c_void_p)]
 
 
 class SpecTreeArgs(ctypes.Structure):
@@ -219,9 +221,15 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
                       kv_capacity: int = 0, eos_token: Optional[int] = None,
                       max_new: Optional[torch.Tensor] = None, top_p: float = 0.0,
+                      gamma_per_request: Optional[torch.Tensor] = None,
+                      temperature_per_request: Optional[torch.Tensor] = None,
+                      top_k_per_request: Optional[torch.Tensor] = None,
+                      top_p_per_request: Optional[torch.Tensor] = None,
                       stream=None) -> None:
     """Marshals one spec_verify_chain call.  Logits are 2-D [rows, V] views
-    (row stride = stride(0)); every tensor must already be on the device."""
+    (row stride = stride(0)); every tensor must already be on the device.
+    The *_per_request tensors (int32 / float32 [B]) give each request its
+    own gamma, temperature, top-k and top-p."""
     V = target_logits.shape[-1]
     B = target_logits.shape[0] // (gamma + 1)
     a = SpecChainArgs(B=B, gamma=gamma, V=V, dtype=_dtype_code(target_logits),
@@ -238,7 +246,10 @@ def spec_verify_chain(*, target_logits: torch.Tensor, draft_tokens: torch.Tensor
                       block_size=int(block_size), kv_capacity=int(kv_capacity),
                       eos_enabled=0 if eos_token is None else 1,
                       eos_token=0 if eos_token is None else int(eos_token), max_new=_ptr(max_new),
-                      top_p=float(top_p))
+                      top_p=float(top_p), gamma_per_request=_ptr(gamma_per_request),
+                      temperature_per_request=_ptr(temperature_per_request),
+                      top_k_per_request=_ptr(top_k_per_request),
+                      top_p_per_request=_ptr(top_p_per_request))
     _check("spec_verify_chain", lib().spec_verify_chain(
         ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream)))
 

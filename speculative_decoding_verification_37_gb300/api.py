@@ -66,6 +66,10 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                  blocks_in_use: Optional[torch.Tensor] = None, block_size: int = 0,
                  kv_capacity: int = 0, eos_token: Optional[int] = None,
                  max_new: Optional[torch.Tensor] = None, top_p: float = 0.0,
+                 gamma_per_request: Optional[torch.Tensor] = None,
+                 temperature_per_request: Optional[torch.Tensor] = None,
+                 top_k_per_request: Optional[torch.Tensor] = None,
+                 top_p_per_request: Optional[torch.Tensor] = None,
                  stream=None) -> ChainOut:
     """target [B*(gamma+1), V], draft [B*gamma, V] (bf16 or f32, rows may be
     strided), draft_tokens int32 [B, gamma], uniforms f32 [B, gamma+1].
@@ -76,11 +80,15 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
     follows, all on the device.  eos_token / max_new (int32 [B] on the
     device) end the round early: its output is cut right after the first
     EOS, then to max_new[b] tokens.  0 < top_p < 1 adds the nucleus after
-    top-k (needs 1 <= top_k <= 128)."""
+    top-k.  The *_per_request tensors (on the device, [B]) give each request
+    its own gamma (<= gamma; the arrays stay padded to gamma), temperature (0:
+    greedy), top-k and top-p."""
     dev = target.device
     V = target.shape[-1]
     B = target.shape[0] // (gamma + 1)
-    sampled = temperature > 0
+    per_request = any(x is not None for x in (gamma_per_request, temperature_per_request,
+                                               top_k_per_request, top_p_per_request))
+    sampled = temperature > 0 or temperature_per_request is not None
     out = ChainOut(
         n_acc=torch.empty(B, dtype=torch.int32, device=dev),
         out_tokens=torch.full((B, gamma + 1), -1, dtype=torch.int32, device=dev),
@@ -91,7 +99,7 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
         if (sampled and residual_mass) else None,
         flags=torch.zeros(B, dtype=torch.int32, device=dev))
     if ws is None:
-        kind = chain_workspace_kind(sampled, top_k, V, residual_mass)
+        kind = L.SPEC_WS_CHAIN if per_request else chain_workspace_kind(sampled, top_k, V, residual_mass)
         ws = workspace(kind, B, gamma, V, dev)
     L.spec_verify_chain(target_logits=target, draft_tokens=draft_tokens, n_acc=out.n_acc,
                         out_tokens=out.out_tokens, n_out=out.n_out, workspace=ws, gamma=gamma,
@@ -101,7 +109,10 @@ def verify_chain(target: torch.Tensor, draft_tokens: torch.Tensor, *, gamma: int
                         committed_len=committed_len, draft_len=draft_len,
                         blocks_in_use=blocks_in_use, block_size=block_size,
                         kv_capacity=kv_capacity, eos_token=eos_token, max_new=max_new,
-                        top_p=top_p, stream=stream)
+                        top_p=top_p, gamma_per_request=gamma_per_request,
+                        temperature_per_request=temperature_per_request,
+                        top_k_per_request=top_k_per_request, top_p_per_request=top_p_per_request,
+                        stream=stream)
     return out
 
 

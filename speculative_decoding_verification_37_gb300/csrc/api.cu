@@ -228,15 +228,20 @@ int chain_args_check(const SpecChainArgs *a) {
         return SPEC_ERR_INVALID_ARG;
     if (!(a->top_p >= 0.0f) || !std::isfinite(a->top_p)) return SPEC_ERR_INVALID_ARG;
     if (a->B == 0) return SPEC_OK;
-    const bool greedy = a->temperature == 0.0f;
+    const bool per_request = a->gamma_per_request || a->temperature_per_request || a->top_k_per_request ||
+                             a->top_p_per_request;
+    const bool greedy = a->temperature == 0.0f && !a->temperature_per_request;
     if (!a->target_logits || a->target_row_stride < a->V) return SPEC_ERR_INVALID_ARG;
     if (!a->n_acc || !a->out_tokens || !a->n_out) return SPEC_ERR_INVALID_ARG;
     if (a->gamma > 0 && !a->draft_tokens) return SPEC_ERR_INVALID_ARG;
     if (!greedy) {
         if (!a->uniforms) return SPEC_ERR_INVALID_ARG;
         if (a->gamma > 0 && (!a->draft_logits || a->draft_row_stride < a->V)) return SPEC_ERR_INVALID_ARG;
-        if (!std::isfinite((float)(1.4426950408889634074 / (double)a->temperature))) return SPEC_ERR_INVALID_ARG;
+        if (!a->temperature_per_request && !std::isfinite((float)(1.4426950408889634074 / (double)a->temperature)))
+            return SPEC_ERR_INVALID_ARG;
     }
+    if (per_request && (a->eos_enabled || a->max_new || a->committed_len))
+        return SPEC_ERR_UNSUPPORTED;  // per-request rounds: no early end, no in-place commit
     const size_t es = esize(a->dtype);
     if (!aligned(a->target_logits, es) || (a->draft_logits && !aligned(a->draft_logits, es)))
         return SPEC_ERR_INVALID_ARG;
@@ -254,7 +259,9 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
     const int chk = chain_args_check(a);
     if (chk != SPEC_OK) return chk;
     if (a->B == 0) return SPEC_OK;
-    const bool greedy = a->temperature == 0.0f;
+    const bool per_request = a->gamma_per_request || a->temperature_per_request || a->top_k_per_request ||
+                             a->top_p_per_request;
+    const bool greedy = a->temperature == 0.0f && !per_request;
     const size_t es = esize(a->dtype);
     InPlace ip{a->committed_len, a->draft_len, a->blocks_in_use, a->block_size, a->kv_capacity};
     const StopRule stop{a->eos_enabled ? a->eos_token : -1, a->max_new};
@@ -342,6 +349,22 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.qcap = (unsigned)(3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32));
         p.ip = ip;
         p.stop = stop;
+        p.rq_gamma = a->gamma_per_request;
+        p.rq_temp = a->temperature_per_request;
+        p.rq_topk = a->top_k_per_request;
+        p.rq_topp = a->top_p_per_request;
+        if (per_request || (nucleus && !(has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax))) {
+            // the exact path: one cluster per position, each request with its own settings
+            // (the scalars stand in for arrays not given)
+            p.per_request = 1;
+            if (a->temperature == 0.0f) {  // a scalar greedy default: no finite 1/T to precompute
+                p.c2 = 0.0f;
+                p.c2lo = 0.0f;
+            }
+            if (rows * p.c > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+            e = launch_chain_sample(p, a->dtype, s);
+            return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+        }
         if (!std::isfinite(p.c2)) return SPEC_ERR_INVALID_ARG;
         // full vocabulary: the persistent kernel when the workspace, the
         // rows' alignment and the sizes allow it
@@ -365,7 +388,6 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         // top-k <= 128: one block per row, kept sets published per position;
         // otherwise the cluster kernel with its exact threshold search
         const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax;
-        if (nucleus && !fast) return SPEC_ERR_UNSUPPORTED;  // the nucleus is cut from the row kernel's kept set
         if (fast) {
             if ((int64_t)a->B * (2 * (int64_t)a->gamma + 1) > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
             e = launch_chain_topk(p, a->dtype, sm_count(), s);

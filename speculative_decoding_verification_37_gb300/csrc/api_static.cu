@@ -44,9 +44,6 @@ extern "C" int spec_verify_chain_static(const SpecChainArgs *a, void *stream) {
     if (a->B == 0) return SPEC_OK;
     const size_t need = spec_workspace_bytes(SPEC_WS_CHAIN, a->B, a->gamma, a->V);
     if (need > kStaticWsBytes) return SPEC_ERR_TOO_LARGE;
-    // top-p is cut from the top-k path's candidate regions, which this
-    // array does not hold
-    if (a->temperature > 0.0f && a->top_p > 0.0f && a->top_p < 1.0f) return SPEC_ERR_UNSUPPORTED;
 
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);

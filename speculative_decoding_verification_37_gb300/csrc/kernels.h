@@ -130,6 +130,13 @@ struct SampleParams {
     unsigned qcap;               // 3*B*(slices the workspace was sized for)
     InPlace ip;
     StopRule stop;
+    // per-request settings (device [B] or null: the scalars above); when
+    // per_request is set the exact cluster path reads them
+    const int *rq_gamma;
+    const float *rq_temp;
+    const int *rq_topk;
+    const float *rq_topp;
+    int per_request;
 };
 
 

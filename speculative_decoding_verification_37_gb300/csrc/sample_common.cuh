@@ -51,6 +51,10 @@ struct SampBase {
     int amb[kAmbMax];             // their indices
     unsigned rej;                 // earliest-rejection word, pushed by rank 0
     int found, lastpos;
+    double redD[kNW];             // the nucleus search: warp totals
+    double nuc_above;             //   mass above the chosen digit, pushed by rank 0
+    unsigned nuc_dig;             //   the chosen digit, pushed by rank 0
+    int nuc_found;
     DdExpTables K;                // the double-float exponential's constants
 };
 
@@ -286,6 +290,72 @@ __device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBas
 }
 
 // ---------------------------------------------------------------------------
+// Per-request settings ("10.6 投机解码" §10.6.3: the requests of a batch
+// accept different lengths; "KV Cache 优化（四）" §4: each request's own
+// processed distributions): the request's gamma, temperature (0: greedy),
+// top-k and top-p, from the per-request arrays when given, else the call's
+// scalars.  A value out of range sets `bad`.
+// ---------------------------------------------------------------------------
+struct ReqCfg {
+    int gamma;     // rows 0..gamma of the request's target, 0..gamma-1 of its draft
+    float c2;      // log2(e) / T
+    float2 it;     // 1 / T as a double-float pair
+    int K;         // top-k (0: keep all)
+    float top_p;   // the nucleus in (0, 1); 0: off
+    bool greedy;
+    unsigned bad;  // SPEC_FLAG_BAD_INPUT for a setting out of range
+};
+
+__device__ __forceinline__ int req_gamma(const SampleParams &p, int b) {
+    if (!p.per_request || !p.rq_gamma) return p.gamma;
+    const int gb = p.rq_gamma[b];
+    return (gb < 0 || gb > p.gamma) ? p.gamma : gb;
+}
+
+__device__ __forceinline__ ReqCfg req_cfg(const SampleParams &p, int b) {
+    ReqCfg c;
+    c.gamma = p.gamma;
+    c.c2 = p.c2;
+    c.it = p.exptab.it;
+    c.K = p.top_k;
+    c.top_p = p.top_p;
+    c.greedy = false;
+    c.bad = 0u;
+    if (!p.per_request) return c;
+    if (p.rq_gamma) {
+        const int gb = p.rq_gamma[b];
+        if (gb < 0 || gb > p.gamma) c.bad = SPEC_FLAG_BAD_INPUT;
+        else c.gamma = gb;
+    }
+    if (p.rq_temp) {
+        const float T = p.rq_temp[b];
+        if (!(T >= 0.0f) || !isfinite(T)) {
+            c.bad = SPEC_FLAG_BAD_INPUT;
+        } else if (T == 0.0f) {
+            c.greedy = true;
+        } else {
+            c.c2 = (float)(1.4426950408889634074 / (double)T);
+            const float hi = __frcp_rn(T);
+            c.it = make_float2(hi, __fmul_rn(__fmaf_rn(-hi, T, 1.0f), hi));  // 1/T = hi + lo to ~2^-46
+            if (!isfinite(c.c2) || !isfinite(hi)) c.bad = SPEC_FLAG_BAD_INPUT;
+        }
+    } else if (p.c2 == 0.0f) {
+        c.greedy = true;  // the scalar temperature is 0
+    }
+    if (p.rq_topk) {
+        const int k = p.rq_topk[b];
+        if (k < 0) c.bad = SPEC_FLAG_BAD_INPUT;
+        c.K = (k < 0 || k >= p.V) ? 0 : k;
+    }
+    if (p.rq_topp) {
+        const float tp = p.rq_topp[b];
+        if (!(tp >= 0.0f)) c.bad = SPEC_FLAG_BAD_INPUT;
+        c.top_p = (tp > 0.0f && tp < 1.0f) ? tp : 0.0f;
+    }
+    return c;
+}
+
+// ---------------------------------------------------------------------------
 // The request epilogue: the last position to arrive writes the outputs.  Run
 // by one warp: lane q reads position q's record (one L2 load each, all in
 // flight together), ballots find the first rejection and any bad input.
@@ -306,17 +376,18 @@ static __device__ void write_request_warp(const SampleParams &p, int b) {
     const PosRec *R = p.recs + (int64_t)b * (g + 1);
     const int len0 = lane == 0 ? inplace_len0(p.ip, b) : 0;
     unsigned badbits = lane == 0 ? inplace_bad(p.ip, len0, g) : 0u;
-    int n = g;  // the first rejecting position (g: all accepted)
+    const int gb = req_gamma(p, b);  // the request's own gamma (records past it are placeholders)
+    int n = gb;  // the first rejecting position (gb: all accepted)
     PosRec mine{};
     for (int q0 = 0; q0 <= g; q0 += 32) {
         const int q = q0 + lane;
         PosRec r{};
         if (q <= g) r = load_rec(R + q);
         if (q0 == 0) mine = r;
-        badbits |= (q <= g && (r.info & REC_BAD_INPUT)) ? SPEC_FLAG_BAD_INPUT : 0u;
-        badbits |= (q <= g && (r.info & REC_BAD_ROW)) ? SPEC_FLAG_BAD_ROW : 0u;
-        const unsigned rej = __ballot_sync(kFull, q < g && !(r.info & REC_ACCEPT));
-        if (n == g && rej) n = q0 + __ffs(rej) - 1;
+        badbits |= (q <= gb && (r.info & REC_BAD_INPUT)) ? SPEC_FLAG_BAD_INPUT : 0u;
+        badbits |= (q <= gb && (r.info & REC_BAD_ROW)) ? SPEC_FLAG_BAD_ROW : 0u;
+        const unsigned rej = __ballot_sync(kFull, q < gb && !(r.info & REC_ACCEPT));
+        if (n == gb && rej) n = q0 + __ffs(rej) - 1;
     }
     badbits = __reduce_or_sync(kFull, badbits);
     if (badbits) {
@@ -340,7 +411,7 @@ static __device__ void write_request_warp(const SampleParams &p, int b) {
             cut = stop_scan(p.stop, q0, q, n, tok, cut);
             if (q <= n) out[q] = (q < lim && q <= cut) ? tok : -1;
             if (q == n && (r.info & REC_FALLBACK)) fb = SPEC_FLAG_FALLBACK;
-            if (q < g) {
+            if (q < gb) {
                 if (p.accept_prob) p.accept_prob[(int64_t)b * g + q] = r.a;
                 if (p.resid) p.resid[(int64_t)b * g + q] = r.z;
             }
@@ -410,6 +481,138 @@ struct SoloEx {
 };
 
 // ---------------------------------------------------------------------------
+// A greedy request's position (temperature 0; "KV Cache 优化（四）" §4): the
+// argmax of target row k over the exchange (lowest index on ties), d_k
+// accepted iff it is that argmax; the argmax is the token the position
+// emits when it ends the round.
+// ---------------------------------------------------------------------------
+template <typename T, typename Ex>
+__device__ void greedy_position(const SampleParams &p, SampBase &sb, Ex &ex, int k, int b, int lo, int hi,
+                                int gamma_b) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, c = ex.c, j = ex.j, g = p.gamma;
+    const bool has_draft = k < gamma_b;
+    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
+    ArgMax am{-INFINITY, -1};
+    for_slice<T, 4>(trow, lo, hi, tid, kNT, [&](float x, int i) {
+        if (am_better(x, i, am.v, am.idx)) am = ArgMax{x, i};
+    });
+    am = warp_argmax(am);
+    if (lane == 0) sb.redd[wid] = make_float4(am.v, __int_as_float(am.idx), 0.0f, 0.0f);
+    __syncthreads();
+    ArgMax t{-INFINITY, -1};
+    if (lane < kNW) t = ArgMax{sb.redd[lane].x, __float_as_int(sb.redd[lane].y)};
+    t = warp_argmax(t);
+    ex.ready();
+    if (tid < c) ex.at(&sb.ms[0], tid)[j] = make_float4(t.v, __int_as_float(t.idx), 0.0f, 0.0f);
+    ex.sync();
+    ArgMax best{-INFINITY, -1};
+    for (int r = 0; r < c; ++r) {
+        const ArgMax x{sb.ms[r].x, __float_as_int(sb.ms[r].y)};
+        if (am_better(x.v, x.idx, best.v, best.idx)) best = x;
+    }
+    if (j == 0) {
+        const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
+        const bool bad_tok = has_draft && (d < 0 || d >= p.V);
+        const bool accept = has_draft && !bad_tok && d == best.idx;
+        Outcome o{accept ? 1.0f : 0.0f, 0.0f, best.idx, (accept ? REC_ACCEPT : 0u) | (bad_tok ? REC_BAD_INPUT : 0u)};
+        finish(p, b, k, o, sb);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The nucleus cut of one row over the exchange: the largest order key tau
+// such that the kept logits (key >= th) at or above tau hold at least top_p
+// of the kept mass, i.e. the key of the first token, by probability, at
+// which the running mass reaches top_p; every token tied with it stays.  A
+// radix descent over 8-bit digits of the key: per digit the masses
+// exp((x - m)/T) (double-float terms, summed in fp64) of the keys that
+// match the prefix so far, gathered in rank 0's shared memory, which picks
+// the digit and pushes it to every CTA.  `dsm` is free (the ring is idle).
+// ---------------------------------------------------------------------------
+template <typename T, typename Ex>
+__device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const T *row, int lo, int hi,
+                                uint32_t th, float m, float top_p) {
+    constexpr int KB = Elem<T>::KEY_BITS;
+    constexpr int KS = 32 - KB;
+    static_assert(kNT == 256, "one digit per thread");
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, c = ex.c, j = ex.j;
+    const DdExpTables &EK = sb.K;
+    double *hist = reinterpret_cast<double *>(dsm);  // [256] this CTA's masses by digit
+    double *all = hist + 256;                        // [kMaxCluster][256], gathered in rank 0
+    uint32_t prefix = 0u;
+    int nb = KB;
+    double above = 0.0, target = 0.0;
+    while (nb > 0) {  // identical in every CTA
+        const int sh = nb > 8 ? nb - 8 : 0;
+        const uint32_t dmask = (1u << (nb - sh)) - 1u;
+        hist[tid] = 0.0;
+        __syncthreads();
+        for_slice<T, 4>(row, lo, hi, tid, kNT, [&](float x, int) {
+            const uint32_t key = fkey(x) >> KS;
+            if (x > -INFINITY && key >= th && (nb == KB || (key >> nb) == (prefix >> nb))) {
+                const dd e = dd_expw(x, m, EK);
+                atomicAdd(&hist[(key >> sh) & dmask], (double)e.hi + (double)e.lo);
+            }
+        });
+        __syncthreads();
+        ex.ready();
+        ex.at(all, 0)[j * 256 + tid] = hist[tid];
+        ex.sync();
+        if (j == 0) {
+            // thread t: digit 255 - t, its mass over the ranks in rank order;
+            // an inclusive scan over t gives the mass of the digits >= 255 - t
+            double v = 0.0;
+            for (int r = 0; r < c; ++r) v += all[r * 256 + (255 - tid)];
+            double incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sb.redD[wid] = incl;
+            __syncthreads();
+            double pre = 0.0, tot = 0.0;
+            for (int w = 0; w < kNW; ++w) {
+                pre += w < wid ? sb.redD[w] : 0.0;
+                tot += sb.redD[w];
+            }
+            if (nb == KB) target = (double)top_p * tot;  // the first digit sees every kept logit
+            const double cum = above + pre + incl;
+            const bool hit = v > 0.0 && cum >= target && cum - v < target;
+            if (tid == 0) sb.nuc_found = 0;
+            __syncthreads();
+            if (hit) {
+                sb.nuc_found = 1;
+                for (int r = 0; r < c; ++r) {
+                    *ex.at(&sb.nuc_dig, r) = 255u - (unsigned)tid;
+                    *ex.at(&sb.nuc_above, r) = cum - v;
+                }
+            }
+            __syncthreads();
+            if (!sb.nuc_found) {
+                // rounding left the mass below top_p: the smallest nonempty digit
+                unsigned lastd = v > 0.0 ? (unsigned)tid + 1u : 0u;
+                lastd = __reduce_max_sync(kFull, lastd);
+                if (lane == 0) sb.redD[wid] = (double)lastd;
+                __syncthreads();
+                unsigned best = 0u;
+                for (int w = 0; w < kNW; ++w) best = max(best, (unsigned)sb.redD[w]);
+                if (best > 0u && tid == (int)best - 1)
+                    for (int r = 0; r < c; ++r) {
+                        *ex.at(&sb.nuc_dig, r) = 255u - (unsigned)tid;
+                        *ex.at(&sb.nuc_above, r) = cum - v;
+                    }
+            }
+        }
+        ex.sync();
+        prefix |= sb.nuc_dig << sh;
+        above = sb.nuc_above;
+        nb = sh;
+    }
+    return prefix;
+}
+
+// ---------------------------------------------------------------------------
 // One position over the exchange `ex`: optional exact top-k threshold by a
 // binary search on order keys (MASK), pass 1 (online max/sum, bulk-copy
 // ring), acceptance, optional fp32 residual mass, and the double-float draw
@@ -424,24 +627,42 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     constexpr int KB = Elem<T>::KEY_BITS;
     constexpr int KS = 32 - KB;
     const int tid = threadIdx.x, c = ex.c, j = ex.j, g = p.gamma;
-    const bool has_draft = k < g;
+    const ReqCfg cfg = req_cfg(p, b);  // identical in every CTA of the exchange
+    if (k > cfg.gamma || cfg.bad) {
+        // a position past the request's own gamma (a placeholder for the
+        // arrival count), or a request whose settings are out of range
+        if (j == 0) {
+            Outcome o{1.0f, 0.0f, -1, REC_ACCEPT | (cfg.bad ? REC_BAD_INPUT : 0u)};
+            finish(p, b, k, o, sb);
+        }
+        return;
+    }
+    if (cfg.greedy) {
+        greedy_position<T>(p, sb, ex, k, b, lo, hi, cfg.gamma);
+        return;
+    }
+    if (p.per_request) {  // this request's 1/T for the double-float exponential
+        if (tid == 0) sb.K.it = cfg.it;
+        __syncthreads();
+    }
+    const bool has_draft = k < cfg.gamma;
     const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
     const T *drow = has_draft
         ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
-    const float c2 = p.c2;
+    const float c2 = cfg.c2;
     const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
     const bool bad_tok = has_draft && (d < 0 || d >= p.V);
     const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
     const float g_d = (has_draft && !bad_tok) ? ld_elem(drow, d) : 0.0f;
     const float u_k = has_draft ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
-    const float u_f = p.unif[(int64_t)b * (g + 1) + g];
+    const float u_f = p.unif[(int64_t)b * (g + 1) + cfg.gamma];
     Outcome o{1.0f, 0.0f, -1, 0u};
 
     uint32_t th_p = 0u, th_q = 0u;
-    if (MASK) {
+    if (MASK && cfg.K > 0) {
         uint32_t lo_p = 0u, hi_p = KB == 32 ? 0xffffffffu : ((1u << KB) - 1u);
         uint32_t lo_q = 0u, hi_q = has_draft ? hi_p : 0u;
-        const unsigned K = (unsigned)p.top_k;
+        const unsigned K = (unsigned)cfg.K;
         for (int it = 0; it < KB; ++it) {
             const bool act_p = lo_p < hi_p, act_q = lo_q < hi_q;
             if (!act_p && !act_q) break;  // identical in every CTA of the exchange
@@ -475,31 +696,43 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     }
 
     // ---- pass 1 (HBM): online max / sum of the kept logits -------------------
-    MaxSum msp{-INFINITY, 0.0f}, msq{-INFINITY, 0.0f};
-    {
-        RingT &R = *reinterpret_cast<RingT *>(dsm);
-        const bool okc = stream_rows<T>(R, trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
-            ms_update<VEC, MASK>(msp, xa, cnt, th_p, KS, c2);
-            if (has_draft) ms_update<VEC, MASK>(msq, xb, cnt, th_q, KS, c2);
-        });
-        if (!okc && tid == 0) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
-    }
-    msp = block_ms<kNT>(msp, c2, sb.red2);
-    msq = block_ms<kNT>(msq, c2, sb.red2);
-    unsigned prior = 0u;
-    if (j == 0 && tid == 0) prior = *((volatile unsigned *)&p.rejword[b]);
-    ex.ready();
-    if (tid < c) {
-        float4 *dst = ex.at(&sb.ms[0], tid);
-        dst[j] = make_float4(msp.m, msp.s, msq.m, msq.s);
-    }
-    if (j == 0 && tid == 0)
-        for (int r = 0; r < c; ++r) *ex.at(&sb.rej, r) = prior;
-    ex.sync();
     MaxSum Mp{-INFINITY, 0.0f}, Mq{-INFINITY, 0.0f};
-    for (int r = 0; r < c; ++r) {
-        Mp = ms_combine(Mp, MaxSum{sb.ms[r].x, sb.ms[r].y}, c2);
-        Mq = ms_combine(Mq, MaxSum{sb.ms[r].z, sb.ms[r].w}, c2);
+    auto pass1 = [&]() {
+        MaxSum msp{-INFINITY, 0.0f}, msq{-INFINITY, 0.0f};
+        {
+            RingT &R = *reinterpret_cast<RingT *>(dsm);
+            const bool okc = stream_rows<T>(R, trow, drow, lo, hi, [&](const float *xa, const float *xb, int, int cnt) {
+                ms_update<VEC, MASK>(msp, xa, cnt, th_p, KS, c2);
+                if (has_draft) ms_update<VEC, MASK>(msq, xb, cnt, th_q, KS, c2);
+            });
+            if (!okc && tid == 0) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+        }
+        msp = block_ms<kNT>(msp, c2, sb.red2);
+        msq = block_ms<kNT>(msq, c2, sb.red2);
+        unsigned prior = 0u;
+        if (j == 0 && tid == 0) prior = *((volatile unsigned *)&p.rejword[b]);
+        ex.ready();
+        if (tid < c) {
+            float4 *dst = ex.at(&sb.ms[0], tid);
+            dst[j] = make_float4(msp.m, msp.s, msq.m, msq.s);
+        }
+        if (j == 0 && tid == 0)
+            for (int r = 0; r < c; ++r) *ex.at(&sb.rej, r) = prior;
+        ex.sync();
+        Mp = MaxSum{-INFINITY, 0.0f};
+        Mq = MaxSum{-INFINITY, 0.0f};
+        for (int r = 0; r < c; ++r) {
+            Mp = ms_combine(Mp, MaxSum{sb.ms[r].x, sb.ms[r].y}, c2);
+            Mq = ms_combine(Mq, MaxSum{sb.ms[r].z, sb.ms[r].w}, c2);
+        }
+    };
+    pass1();
+    if (MASK && cfg.top_p > 0.0f && Mp.m > -INFINITY && (!has_draft || Mq.m > -INFINITY)) {
+        // top-p after temperature and top-k ("KV Cache 优化（四）" §4): each
+        // row's threshold becomes its nucleus cut, then pass 1 again
+        th_p = nucleus_key<T, Ex>(ex, sb, dsm, trow, lo, hi, th_p, Mp.m, cfg.top_p);
+        if (has_draft) th_q = nucleus_key<T, Ex>(ex, sb, dsm, drow, lo, hi, th_q, Mq.m, cfg.top_p);
+        pass1();
     }
     const bool bad_row = Mp.m == -INFINITY || (has_draft && Mq.m == -INFINITY);
     const bool bad = bad_tok || bad_row;

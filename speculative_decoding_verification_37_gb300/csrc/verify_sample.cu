@@ -39,7 +39,6 @@ template <typename T, bool MASK>
 __global__ void __launch_bounds__(kNT, 3) chain_sample_kernel(SampleParams p) {
     __shared__ SampBase sb;
     extern __shared__ __align__(128) unsigned char dsm[];
-    const int tid = threadIdx.x;
     load_exp_tables(p, sb);
     __syncthreads();
     // Every CTA of the cluster must have started (and initialised the shared
@@ -75,7 +74,7 @@ cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const bool mask = p.top_k > 0;
+    const bool mask = p.top_k > 0 || p.per_request;  // per-request top-k and top-p need the masked path
     if (dtype == SPEC_DTYPE_BF16)
         return mask ? launch_mask<__nv_bfloat16, true>(cfg, p) : launch_mask<__nv_bfloat16, false>(cfg, p);
     return mask ? launch_mask<float, true>(cfg, p) : launch_mask<float, false>(cfg, p);

@@ -37,7 +37,7 @@
 //     writes the request's outputs.
 // A row whose candidates do not fit (hundreds of logits tied at the
 // threshold) sends its position to the exact masked computation over both
-// rows in the deciding block (slow, exact, rare).
+// rows in the deciding block, the nucleus included (slow, exact, rare).
 #include "sample_common.cuh"
 
 namespace specv {
@@ -756,15 +756,7 @@ __global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_row_kernel(Sam
             __syncthreads();
             const bool exact = ((D.flags[0] | (k < g ? D.flags[1] : 0u)) & RK_OVERFLOW) != 0u;  // block-uniform
             if (exact) {
-                if (nucleus) {
-                    // the masked path has no nucleus: the position is flagged
-                    if (wid == 0) {
-                        Outcome o{1.0f, 0.0f, -1, REC_BAD_ROW};
-                        finish(p, b, k, o, sb);
-                    }
-                } else {
-                    rk_exact_position<T>(p, sb, dsm, k, b);
-                }
+                rk_exact_position<T>(p, sb, dsm, k, b);
             } else {
                 const Outcome o = block_outcome<T>(p, b, k, D, EK, rd, &s_rej);
                 finish(p, b, k, o, sb);

@@ -57,6 +57,8 @@ def test_struct_layouts_match_c(lib):
         P(SpecChainArgs, flags) P(SpecChainArgs, fallback_eps) P(SpecChainArgs, uniforms)
         P(SpecChainArgs, committed_len) P(SpecChainArgs, block_size) P(SpecChainArgs, kv_capacity)
         P(SpecChainArgs, eos_enabled) P(SpecChainArgs, max_new) P(SpecChainArgs, top_p)
+        P(SpecChainArgs, gamma_per_request) P(SpecChainArgs, temperature_per_request)
+        P(SpecChainArgs, top_k_per_request) P(SpecChainArgs, top_p_per_request)
         P(SpecTreeArgs, flags) P(SpecTreeArgs, committed_len) P(SpecTreeArgs, row_stride)
         P(SpecCommitArgs, flags) P(SpecCommitArgs, num_blocks) P(SpecCommitArgs, slots_stride)
         return 0;
@@ -133,8 +135,7 @@ def test_static_entry_point_checks_arguments_first(lib, bad):
     of its array) would fail with SPEC_ERR_CUDA instead."""
     a = _chain_args(**bad)
     assert lib.spec_verify_chain_static(ctypes.byref(a), None) == L.SPEC_ERR_INVALID_ARG
-    # top-p needs the candidate regions the fixed array does not hold
-    a = _chain_args(top_p=0.9, top_k=5)
+    a = _chain_args(gamma_per_request=8192, eos_enabled=1, eos_token=3)
     assert lib.spec_verify_chain_static(ctypes.byref(a), None) == L.SPEC_ERR_UNSUPPORTED
     assert lib.spec_verify_chain_static(ctypes.byref(_chain_args(B=0)), None) == L.SPEC_OK
 
@@ -221,15 +222,13 @@ def test_tree_level_children_limits(lib):
     assert L.spec_workspace_bytes(L.SPEC_WS_TREE_LEVEL, 128, 2, 128256) >= 128 * 2 * 32 * 144
 
 
-def test_top_p_needs_the_top_k_path(lib):
-    """The nucleus is built in the top-k merge: top_p without 1 <= top_k <= 128
-    is refused before anything is launched."""
-    for top_k in (0, 129):
-        a = _chain_args(top_p=0.9, top_k=top_k)
-        n = L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 2, 2, 16)
-        ws = ctypes.create_string_buffer(n + 256)
-        base = (ctypes.addressof(ws) + 255) // 256 * 256
-        assert lib.spec_verify_chain(ctypes.byref(a), ctypes.c_void_p(base), n, None) == L.SPEC_ERR_UNSUPPORTED
+def test_per_request_rounds_have_no_early_end(lib):
+    """Per-request settings go with neither the early end of a round nor the
+    in-place commit: refused before anything is launched."""
+    ws = ctypes.create_string_buffer(1 << 16)
+    for over in (dict(eos_enabled=1, eos_token=3), dict(max_new=4096), dict(committed_len=4096)):
+        a = _chain_args(gamma_per_request=8192, **over)
+        assert lib.spec_verify_chain(ctypes.byref(a), ws, 1 << 16, None) == L.SPEC_ERR_UNSUPPORTED
 
 
 def test_workspace_cache_and_clear(lib):

@@ -91,20 +91,26 @@ def test_static_scratch_rejects_oversized_batches():
     assert np.isfinite(need)
 
 
-def test_static_scratch_refuses_top_p_before_enqueuing():
-    """Top-p is cut from the top-k path's candidate regions, which the fixed
-    array does not hold: such a call is refused up front."""
+def test_static_scratch_with_top_p_matches_the_workspace_entry_point():
+    """Top-p through the fixed array: the exact path, with the same results
+    as the workspace entry point taking that path with a plain workspace."""
     _build.build()
     spec = CASES["topk"]
     dev = "cuda"
     batch = W.make_chain(spec, seed=3)
+    common = dict(target_logits=batch.target.to(dev),
+                  draft_tokens=torch.from_numpy(batch.draft_tokens).to(dev), gamma=spec.gamma,
+                  temperature=spec.temperature, draft_logits=batch.draft.to(dev),
+                  uniforms=torch.from_numpy(batch.uniforms).to(dev), top_k=spec.top_k, top_p=0.9)
+    ref = _outputs(spec.B, spec.gamma, True, dev)
+    L.spec_verify_chain(workspace=api.workspace(L.SPEC_WS_CHAIN, spec.B, spec.gamma, spec.V, dev),
+                        **common, **ref)
     got = _outputs(spec.B, spec.gamma, True, dev)
-    with pytest.raises(RuntimeError, match="unsupported"):
-        L.spec_verify_chain_static(target_logits=batch.target.to(dev),
-                                   draft_tokens=torch.from_numpy(batch.draft_tokens).to(dev),
-                                   gamma=spec.gamma, temperature=spec.temperature,
-                                   draft_logits=batch.draft.to(dev),
-                                   uniforms=torch.from_numpy(batch.uniforms).to(dev),
-                                   top_k=spec.top_k, top_p=0.9, **got)
     torch.cuda.synchronize()
-    assert int(got["n_out"].min()) == -7  # nothing ran
+    free0 = torch.cuda.mem_get_info()[0]
+    L.spec_verify_chain_static(**common, **got)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    for key in ("n_acc", "n_out", "out_tokens", "flags"):
+        assert torch.equal(got[key], ref[key]), key
+    assert int(got["n_out"].min()) >= 1
