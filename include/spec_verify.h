@@ -370,6 +370,16 @@ const char *spec_error_string(int code);
 /* Text of the last CUDA error a call of this library saw on this thread. */
 const char *spec_last_cuda_error(void);
 
+/* How many idle polls (about 0.5 us each) a warp of the persistent
+ * full-vocabulary chain path makes, while none of its work is ready, before
+ * it gives up: it leaves once the copies it has in flight have landed, and
+ * the call sets SPEC_FLAG_TIMEOUT (its outputs are then not valid and the
+ * workspace must be zeroed again).  polls <= 0 restores the default, 2^21
+ * (about a second).  Process-wide, read when a call is made; meant for
+ * tests of the timeout path.  Always SPEC_OK.  (The pages have no
+ * counterpart: this bounds a wait of this implementation.) */
+int spec_set_idle_limit(int64_t polls);
+
 /*
  * N-gram (prompt-lookup) drafts, a model-free draft source ("10.6 投机解码"
  * §10.6.3 实际部署; "KV Cache 优化（四）" §10.2 N-gram 或前缀匹配): for each

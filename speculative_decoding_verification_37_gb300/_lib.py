@@ -28,7 +28,8 @@ TOPK_FAST_MAX = 128   # top_k served by the candidate-pool path when the workspa
 
 EXPORTED = ("spec_verify_chain", "spec_verify_tree", "spec_commit_kv", "spec_workspace_bytes",
             "spec_get_status", "spec_error_string", "spec_last_cuda_error",
-            "spec_verify_chain_static", "spec_selftest_ex2", "spec_ngram_draft", "spec_tree_level")
+            "spec_verify_chain_static", "spec_selftest_ex2", "spec_ngram_draft", "spec_tree_level",
+            "spec_set_idle_limit")
 
 
 class SpecChainArgs(ctypes.Structure):
@@ -119,6 +120,8 @@ def lib():
         L.spec_last_cuda_error.restype = c_char_p
         L.spec_selftest_ex2.argtypes = [POINTER(ctypes.c_float)]
         L.spec_selftest_ex2.restype = c_int
+        L.spec_set_idle_limit.argtypes = [c_int64]
+        L.spec_set_idle_limit.restype = c_int
         L.spec_ngram_draft.argtypes = [POINTER(SpecNgramArgs), c_void_p]
         L.spec_ngram_draft.restype = c_int
         L.spec_tree_level.argtypes = [POINTER(SpecTreeLevelArgs), c_void_p, c_size_t, c_void_p]
@@ -200,6 +203,12 @@ def spec_selftest_ex2() -> float:
     out = ctypes.c_float(0.0)
     _check("spec_selftest_ex2", lib().spec_selftest_ex2(ctypes.byref(out)))
     return float(out.value)
+
+
+def spec_set_idle_limit(polls: int) -> None:
+    """Idle polls before a warp of the persistent full-vocabulary path gives
+    up (SPEC_FLAG_TIMEOUT); 0 restores the default.  Process-wide."""
+    _check("spec_set_idle_limit", lib().spec_set_idle_limit(int(polls)))
 
 
 def spec_get_status(workspace: torch.Tensor, stream=None) -> int:

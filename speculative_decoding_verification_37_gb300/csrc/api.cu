@@ -14,6 +14,7 @@ using namespace specv;
 namespace {
 
 thread_local char g_cuda_err[256] = "";
+std::atomic<long long> g_idle_limit{0};  // 0: the full-vocabulary path's default
 
 int cuda_fail(cudaError_t e) {
     std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -349,6 +350,10 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.qcap = (unsigned)(3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32));
         p.ip = ip;
         p.stop = stop;
+        {
+            const long long lim = g_idle_limit.load(std::memory_order_relaxed);
+            p.idle_limit = lim > 0 ? lim : full_idle_limit();
+        }
         p.rq_gamma = a->gamma_per_request;
         p.rq_temp = a->temperature_per_request;
         p.rq_topk = a->top_k_per_request;
@@ -567,3 +572,8 @@ extern "C" const char *spec_error_string(int code) {
 }
 
 extern "C" const char *spec_last_cuda_error(void) { return g_cuda_err; }
+
+extern "C" int spec_set_idle_limit(int64_t polls) {
+    g_idle_limit.store(polls > 0 ? (long long)polls : 0, std::memory_order_relaxed);
+    return SPEC_OK;
+}

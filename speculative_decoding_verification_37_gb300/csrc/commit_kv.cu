@@ -130,11 +130,14 @@ __global__ void __launch_bounds__(32) commit_kv_kernel(CommitParams p) {
         bulk_commit();
         bulk_wait_read();  // the stage may go; the writes finish before the kernel does
     } else {
-        // the loads are still outstanding: give them one more bounded wait
-        // before the block (and its shared memory) goes away
-        mbar_wait_bounded(&bar, 0u);
+        // the loads are still outstanding: wait for them (bounded) before the
+        // block (and its shared memory) goes away
+        // (then no arrival: the length does not advance past a group that
+        // was not copied)
+        if (mbar_drain(&bar, 0u)) mbar_inval(&bar);  // otherwise the barrier stays as it is
         if (p.flags) atomicOr(p.flags + b, SPEC_FLAG_TIMEOUT);
         atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+        return;
     }
     mbar_inval(&bar);
 

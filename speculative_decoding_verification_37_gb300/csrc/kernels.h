@@ -137,6 +137,7 @@ struct SampleParams {
     const int *rq_topk;
     const float *rq_topp;
     int per_request;
+    long long idle_limit;  // full-vocabulary path: idle polls before a warp gives up
 };
 
 
@@ -189,6 +190,7 @@ int argmax_stage_bytes();  // a greedy slice body must fit this
 cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s);
 cudaError_t launch_chain_full(const SampleParams &p, int dtype, int sms, cudaStream_t s);
+long long full_idle_limit();  // the default of SampleParams::idle_limit
 int full_row_bytes();   // one row's slice of the full-vocabulary path
 int full_max_slices();  // slices per row it supports
 int topk_row_bytes();  // a top-k slice body per row must fit this

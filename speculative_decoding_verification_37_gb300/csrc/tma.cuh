@@ -69,6 +69,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsig
     return false;
 }
 
+// After a wait ran out: waits (bounded, four times the normal limit) for a
+// stage whose bulk copy was issued and not yet seen complete, so that no copy
+// lands in shared memory after the block has moved on or exited.  False if
+// even that ran out; the caller then leaves the barrier as it is.
+__device__ __forceinline__ bool mbar_drain(unsigned long long *bar, unsigned phase) {
+    for (int rep = 0; rep < 4; ++rep)
+        if (mbar_wait_bounded(bar, phase)) return true;
+    return false;
+}
+
 // bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
 __device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes,
                                          unsigned long long *bar) {
@@ -148,22 +158,34 @@ __device__ bool ring_stream(Ring<CH, NST, ROWS> &R, const unsigned char *const *
         for (int s = 0; s < NST && s < nch; ++s) issue(s, s);
     }
     __syncthreads();
-    bool ok = true;
     for (int i = 0; i < nch; ++i) {
         const int s = i % NST;
-        ok &= mbar_wait_bounded(&R.full[s], (unsigned)((i / NST) & 1));
+        const bool ok = mbar_wait_bounded(&R.full[s], (unsigned)((i / NST) & 1));
         const unsigned char *stage[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) stage[r] = R.buf[s][r];
         const uint32_t off = (uint32_t)i * CH;
         f(stage, off, min((uint32_t)CH, nbytes - off));
-        __syncthreads();
+        if (__syncthreads_or(!ok)) {
+            // a chunk did not arrive in time: issue nothing more, wait for
+            // the chunks already issued (i .. i+NST-1) before the ring's
+            // memory may be used again, and report the failure
+            if (threadIdx.x == 0) {
+                bool drained = true;
+                for (int q = i; q < nch && q < i + NST; ++q)
+                    drained &= mbar_drain(&R.full[q % NST], (unsigned)((q / NST) & 1));
+                if (drained)
+                    for (int t = 0; t < NST; ++t) mbar_inval(&R.full[t]);
+            }
+            __syncthreads();
+            return false;
+        }
         if (threadIdx.x == 0 && i + NST < nch) issue(i + NST, s);
     }
     if (threadIdx.x == 0)
         for (int s = 0; s < NST; ++s) mbar_inval(&R.full[s]);
     __syncthreads();
-    return ok;
+    return true;
 }
 
 // Split of a row slice [lo, hi) into scalar head, 16-byte body, scalar tail.

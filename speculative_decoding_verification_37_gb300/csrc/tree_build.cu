@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kTlWarps * 32, 2) tree_level_kernel(const Tree
         if (lane == 0) {
             atomicOr(p.status, SPEC_FLAG_TIMEOUT);
             for (int u = t; u < mine && u < t + NST; ++u) {
-                mbar_wait_bounded(&bar[st], phase);
+                mbar_drain(&bar[st], phase);
                 if (++st == NST) {
                     st = 0;
                     phase ^= 1u;

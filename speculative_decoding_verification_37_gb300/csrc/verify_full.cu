@@ -59,6 +59,7 @@ constexpr int kFwAmb = kFullAmb;       // in-band residual elements listed per (
 constexpr int kFwGroup0 = 4;           // slices per queue item, fp32 round
 constexpr int kFwGroupDD = 1;          // slices per queue item, double-float rounds
 constexpr long long kFwIdleLimit = 1ll << 21;  // idle polls (about 0.5 us each) before giving up
+long long full_idle_limit() { return kFwIdleLimit; }
 
 // ---- the certified fp32 round's error model --------------------------------
 // A term 2^((x - m) c) is computed with its exponent exact to ~2^-48 (x - m by
@@ -383,7 +384,7 @@ __device__ __noinline__ void fu_decide(const SampleParams &p, int pos) {
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ int fw_stream(const SampleParams &p, FwRing &R, unsigned long long *full, int t, int s, int GW,
-                         unsigned &phase, bool &timeout, int &slice) {
+                         unsigned &phase, bool &timeout, int &slice, int &issued) {
     constexpr int VEC = Elem<T>::VEC;
     const int lane = threadIdx.x & 31;
     const int g = p.gamma, c = p.c;
@@ -397,7 +398,8 @@ __device__ int fw_stream(const SampleParams &p, FwRing &R, unsigned long long *f
     const float c2 = p.c2;
     int d = -1;
     if (k < g && lane == 0) d = p.tokens[(int64_t)b * g + k];
-    if (!mbar_wait_bounded(&full[s], (phase >> s) & 1u)) timeout = true;
+    const bool landed = mbar_wait_bounded(&full[s], (phase >> s) & 1u);
+    if (!landed) timeout = true;
     phase ^= 1u << s;
     float2 res[2] = {make_float2(-INFINITY, 0.0f), make_float2(-INFINITY, 0.0f)};
 #pragma unroll
@@ -441,7 +443,11 @@ __device__ int fw_stream(const SampleParams &p, FwRing &R, unsigned long long *f
     __syncwarp();  // every lane is done with stage s
     if (lane == 0) {
         const int nt = t + kFwNST * GW;
-        if (nt < p.B * (g + 1) * c) fw_issue<T>(p, R, full, nt, s);
+        // (after a copy that did not land, nothing more is issued)
+        if (nt < p.B * (g + 1) * c && !timeout) {
+            fw_issue<T>(p, R, full, nt, s);
+            ++issued;
+        }
         p.fpart[((int64_t)pos * 2) * c + j] = res[0];
         if (rows > 1) p.fpart[((int64_t)pos * 2 + 1) * c + j] = res[1];
         if (stash) p.fxd[pos] = xd;
@@ -1186,12 +1192,16 @@ __global__ void __launch_bounds__(kFwWarps * 32, 1) chain_full_kernel(SamplePara
         for (int i = threadIdx.x; i < NW; i += blockDim.x) dst[i] = src[i];
     }
     int t = (int)blockIdx.x * kFwWarps + w, it = 0;
+    int issued = 0;  // lane 0: stream items of this warp whose copies were issued
     if (lane == 0) {
         for (int s = 0; s < kFwNST; ++s) mbar_init(&fb[s], 1);
         fence_barrier_init();
         for (int s = 0; s < kFwNST; ++s) {
             const int ts = t + s * GW;
-            if (ts < nitems) fw_issue<T>(p, R, fb, ts, s);
+            if (ts < nitems) {
+                fw_issue<T>(p, R, fb, ts, s);
+                ++issued;
+            }
         }
     }
     __syncthreads();  // the exponential's tables; from here on warps are independent
@@ -1251,7 +1261,7 @@ __global__ void __launch_bounds__(kFwWarps * 32, 1) chain_full_kernel(SamplePara
             if (cmd < 0) {
                 if (wh == wt && nfin_pf >= (unsigned)p.B) {
                     cmd = kCmdDone;
-                } else if (++idle > kFwIdleLimit) {
+                } else if (++idle > p.idle_limit) {
                     timeout = true;
                     cmd = kCmdDone;
                 } else {
@@ -1278,7 +1288,11 @@ __global__ void __launch_bounds__(kFwWarps * 32, 1) chain_full_kernel(SamplePara
         if (cmd == kCmdDone) break;
         if (cmd == kCmdStream) {
             int j = 0;
-            const int pos = fw_stream<T>(p, R, fb, t, it % kFwNST, GW, phase, timeout, j);
+            const int pos = fw_stream<T>(p, R, fb, t, it % kFwNST, GW, phase, timeout, j, issued);
+            if (__shfl_sync(kFull, timeout ? 1 : 0, 0)) {  // a copy did not land: stop
+                ++it;
+                break;
+            }
             if (lane == 0) {
                 due = p.pcnt + pos;
                 due_n = 1u;
@@ -1310,7 +1324,15 @@ __global__ void __launch_bounds__(kFwWarps * 32, 1) chain_full_kernel(SamplePara
     __syncwarp();
     if (lane == 0) {
         if (timeout) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
-        for (int s = 0; s < kFwNST; ++s) mbar_inval(&fb[s]);
+        // copies issued and not consumed (a wait gave up, or the warp left on
+        // the idle limit with items ahead): wait for them (bounded) before
+        // the block's shared memory may be reused, from the last item whose
+        // wait may have failed
+        bool drained = true;
+        for (int q = timeout ? it - 1 : it; q < issued; ++q)
+            if (q >= 0) drained &= mbar_drain(&fb[q % kFwNST], (unsigned)((q / kFwNST) & 1));
+        if (drained)
+            for (int s = 0; s < kFwNST; ++s) mbar_inval(&fb[s]);
         __threadfence();
         if (atomicAdd(&ctl->nexit, 1u) == (unsigned)(GW - 1)) {
             ctl->head = 0u;

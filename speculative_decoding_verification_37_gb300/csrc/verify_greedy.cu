@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kArgNT, kArgBlocksPerSM) argmax_pass_kernel(Ar
         const int nhead = sp.body0 - sp.head0, ntail = sp.hi - sp.tail0;
         const float xh = tid < nhead ? ld_elem(r, sp.head0 + tid) : -INFINITY;
         const float xt = tid < ntail ? ld_elem(r, sp.tail0 + tid) : -INFINITY;
-        if (!mbar_wait_bounded(&full[s], (phase >> s) & 1u)) timeout = true;
+        const bool ok = mbar_wait_bounded(&full[s], (phase >> s) & 1u);
         phase ^= 1u << s;
         const int nvec = (sp.tail0 - sp.body0) / VEC;
         const uint4 *v = reinterpret_cast<const uint4 *>(R.buf[s]);
@@ -305,7 +305,22 @@ __global__ void __launch_bounds__(kArgNT, kArgBlocksPerSM) argmax_pass_kernel(Ar
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine = min(mine, __shfl_xor_sync(kFull, mine, o));
         if (lane == 0) s_i[w] = mine;
-        __syncthreads();  // stage s is consumed
+        if (__syncthreads_or(!ok)) {  // stage s is consumed; a copy did not arrive in time
+            // issue nothing more; wait for the copies already issued (this
+            // block's local items t .. t+NST-1) before the block may exit
+            if (tid == 0) {
+                bool drained = true;
+                int u = t;
+                for (int nxt = item; nxt < n_items && u < t + kArgNST; nxt += G, ++u)
+                    drained &= mbar_drain(&full[u % kArgNST], (unsigned)((u / kArgNST) & 1));
+                atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+                timeout = !drained;  // true: leave the barriers as they are
+            }
+            __syncthreads();
+            if (tid == 0 && !timeout)
+                for (int q = 0; q < kArgNST; ++q) mbar_inval(&full[q]);
+            return;
+        }
         if (tid == 0) {
             int best = s_i[0];
 #pragma unroll
@@ -314,7 +329,6 @@ __global__ void __launch_bounds__(kArgNT, kArgBlocksPerSM) argmax_pass_kernel(Ar
             if (item + kArgNST * G < n_items) arg_issue<T>(p, R, full, item + kArgNST * G, s);
         }
     }
-    if (timeout) atomicOr(p.status, SPEC_FLAG_TIMEOUT);
     __syncthreads();
     if (tid == 0)
         for (int s = 0; s < kArgNST; ++s) mbar_inval(&full[s]);
