@@ -134,7 +134,13 @@ extern "C" {
  *   holds spec_workspace_bytes(SPEC_WS_CHAIN_FULL, B, gamma, V) bytes, rows
  *   and strides are 16-byte aligned, V * element size is a multiple of 16,
  *   gamma <= 30, V * element size <= 1 MiB and the call has at least 1,024
- *   (row, 4 KiB slice) items; otherwise the cluster kernel.
+ *   (row, 4 KiB slice) items; otherwise the cluster kernel.  The first such
+ *   call on a device first re-measures the error bound of the hardware
+ *   exponential that the certified draw assumes (spec_selftest_ex2;
+ *   synchronous, about a second: the one place this call synchronises); a
+ *   device outside the bound never takes the persistent path, and a call
+ *   made while the stream is being captured before that measurement takes
+ *   the cluster kernel.
  *   All paths give identical results up to the stated tolerances.
  */
 typedef struct SpecChainArgs {

@@ -25,6 +25,24 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t esize(int dtype) { return dtype == SPEC_DTYPE_BF16 ? 2 : 4; }
 
+// Whether this device's hardware exponential keeps within the error bound
+// the full-vocabulary path's certified fp32 draw assumes, measured once per
+// device by the exhaustive self-test (synchronous, about a second).  Not
+// measured while `s` is being captured: such a call takes another path.
+bool ex2_certified(cudaStream_t s) {
+    static std::atomic<int> state[64];  // 0 unknown, 1 within the bound, 2 not
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const int st = state[dev].load(std::memory_order_acquire);
+    if (st != 0) return st == 1;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return false;
+    float worst = 1.0f;
+    const bool ok = spec_selftest_ex2(&worst) == SPEC_OK && worst <= full_ex2_bound();
+    state[dev].store(ok ? 1 : 2, std::memory_order_release);
+    return ok;
+}
+
 int sm_count() {
     static std::atomic<int> cached[64];
     int dev = 0, n = 0;
@@ -382,7 +400,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
                           aligned(a->target_logits, 16) && (a->target_row_stride * (int64_t)es) % 16 == 0 &&
                           (a->gamma == 0 || (aligned(a->draft_logits, 16) &&
                                              (a->draft_row_stride * (int64_t)es) % 16 == 0));
-        if (full) {
+        if (full && ex2_certified(s)) {
             p.c = full_slices(a->V, a->dtype);
             p.Vs = full_row_bytes() / (int)es;
             if (rows * p.c > 0x7fffffffLL / 3 || 3 * (int64_t)a->B * full_slices(a->V, SPEC_DTYPE_F32) > 0x7fffffffLL)

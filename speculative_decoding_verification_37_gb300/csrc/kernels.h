@@ -191,6 +191,7 @@ cudaError_t launch_chain_sample(const SampleParams &p, int dtype, cudaStream_t s
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s);
 cudaError_t launch_chain_full(const SampleParams &p, int dtype, int sms, cudaStream_t s);
 long long full_idle_limit();  // the default of SampleParams::idle_limit
+float full_ex2_bound();       // the hardware exponential's relative error the certified draw assumes
 int full_row_bytes();   // one row's slice of the full-vocabulary path
 int full_max_slices();  // slices per row it supports
 int topk_row_bytes();  // a top-k slice body per row must fit this

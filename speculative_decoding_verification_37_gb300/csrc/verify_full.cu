@@ -72,6 +72,7 @@ long long full_idle_limit() { return kFwIdleLimit; }
 // neglected exponent and second-order terms.
 constexpr float kU = 5.9604644775390625e-8f;  // 2^-24
 constexpr float kEx2Err = 1.5e-7f;
+float full_ex2_bound() { return kEx2Err; }
 constexpr float kTermErr = kEx2Err + 0.5f * kU + 1e-10f;
 // A slice sum: pairwise within a 16-byte vector (depth <= 3, plain fp32),
 // then compensated (TwoSum) across vectors and lanes and kept as a
