@@ -353,7 +353,7 @@ def kernel_name(wl: Workload) -> str:
     if wl.kind == "tree" or wl.spec.greedy:
         return "argmax_pass_kernel+argmax_decide_kernel"
     if 0 < wl.spec.top_k <= L.TOPK_FAST_MAX:
-        return "chain_topk_row_kernel"
+        return "chain_topk_pass_kernel+chain_topk_decide_kernel"
     if (wl.spec.top_k == 0 or wl.spec.top_k >= wl.spec.V) and \
             wl.rows * -(-wl.spec.V * wl.spec.esize // 4096) >= 1024:
         return "chain_full_kernel"  # the persistent full-vocabulary path (at least 1,024 4 KiB items)

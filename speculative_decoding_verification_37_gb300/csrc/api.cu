@@ -74,9 +74,8 @@ struct Ws {
     unsigned *counters;  // [B] arrival counters
     unsigned *rejword;   // [B] earliest rejection per request (chain, sampled)
     void *data;          // chain: records or argmax keys; tree: argmax keys
-    TopkRow *rkrow;      // chain, top-k: [B*(gamma+1)][2] published kept-set headers
-    uint2 *rkent;        // chain, top-k: [B*(gamma+1)][2][kKeptRowMax] kept entries
-    unsigned *rkcnt;     // chain, top-k: [B*(gamma+1)] position arrival counters (zeroed)
+    uint32_t *rkmax;     // chain, top-k: [B*(gamma+1)*2][kTopKThreads] thread maxima
+    uint32_t *rkgrp;     // chain, top-k: [B*(gamma+1)*2][kTopKGroups][kTopKThreads] largest groups
     // chain, full vocabulary: see SampleParams
     float2 *fpart, *fxd;
     float4 *fstat;
@@ -119,13 +118,11 @@ size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_
         return at;
     };
     if (extra == kWsPool) {
-        char *rc = take(rows * sizeof(unsigned));
-        char *rh = take(rows * 2 * sizeof(TopkRow));
-        char *re = take(rows * 2 * (size_t)kKeptRowMax * sizeof(uint2));
+        char *rm = take(rows * 2 * (size_t)kTopKThreads * sizeof(uint32_t));
+        char *rg = take(rows * 2 * (size_t)kTopKGroups * kTopKThreads * sizeof(uint32_t));
         if (w) {
-            w->rkcnt = reinterpret_cast<unsigned *>(rc);
-            w->rkrow = reinterpret_cast<TopkRow *>(rh);
-            w->rkent = reinterpret_cast<uint2 *>(re);
+            w->rkmax = reinterpret_cast<uint32_t *>(rm);
+            w->rkgrp = reinterpret_cast<uint32_t *>(rg);
         }
     } else if (extra == kWsFull) {
         const size_t c = (size_t)full_slices(V, SPEC_DTYPE_F32), nb = (size_t)B;
@@ -352,9 +349,8 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.counters = w.counters;
         p.rejword = w.rejword;
         p.recs = static_cast<PosRec *>(w.data);
-        p.rkrow = w.rkrow;
-        p.rkent = w.rkent;
-        p.rkcnt = w.rkcnt;
+        p.rkmax = w.rkmax;
+        p.rkgrp = w.rkgrp;
         p.fpart = w.fpart;
         p.fxd = w.fxd;
         p.fstat = w.fstat;
@@ -376,7 +372,10 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.rq_temp = a->temperature_per_request;
         p.rq_topk = a->top_k_per_request;
         p.rq_topp = a->top_p_per_request;
-        if (per_request || (nucleus && !(has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax))) {
+        // the top-k path: top_k <= 128, chunk indices within 16 bits
+        const bool topk_fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax &&
+                               ((int64_t)a->V * (int64_t)es + topk_row_bytes() - 1) / topk_row_bytes() <= 0xffff;
+        if (per_request || (nucleus && !topk_fast)) {
             // the exact path: one cluster per position, each request with its own settings
             // (the scalars stand in for arrays not given)
             p.per_request = 1;
@@ -410,8 +409,7 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         }
         // top-k <= 128: one block per row, kept sets published per position;
         // otherwise the cluster kernel with its exact threshold search
-        const bool fast = has_pool && p.top_k > 0 && p.top_k <= kTopKFastMax;
-        if (fast) {
+        if (topk_fast) {
             if ((int64_t)a->B * (2 * (int64_t)a->gamma + 1) > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
             e = launch_chain_topk(p, a->dtype, sm_count(), s);
         } else {

@@ -152,6 +152,36 @@ __device__ __forceinline__ void for_slice_vec(const T *row, int lo, int hi, int 
 }
 
 // ---------------------------------------------------------------------------
+// Barriers of the first NT threads of a block (named barrier 1).  In a block
+// of exactly NT threads they act as __syncthreads (and its count / or
+// forms); in a block that adds a producer warp after the first NT threads,
+// they synchronise the other threads only, so the producer never waits.
+// ---------------------------------------------------------------------------
+template <int NT> __device__ __forceinline__ void sync_nt() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+template <int NT> __device__ __forceinline__ int sync_nt_count(bool pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.popc.u32 %0, 1, %2, p;\n\t}"
+        : "=r"(r)
+        : "r"((int)pred), "n"(NT)
+        : "memory");
+    return r;
+}
+template <int NT> __device__ __forceinline__ bool sync_nt_or(bool pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((int)pred), "n"(NT)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------------------
 // reductions (fixed combination order, hence deterministic)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
@@ -165,9 +195,9 @@ __device__ __forceinline__ unsigned warp_sum_u(unsigned v) { return __reduce_add
 template <int NT> __device__ __forceinline__ float block_sum(float v, float *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum(v);
-    __syncthreads();
+    sync_nt<NT>();
     if (lane == 0) red[w] = v;
-    __syncthreads();
+    sync_nt<NT>();
     float t = lane < NT / 32 ? red[lane] : 0.0f;
     return warp_sum(t);
 }
@@ -175,9 +205,9 @@ template <int NT> __device__ __forceinline__ float block_sum(float v, float *red
 template <int NT> __device__ __forceinline__ unsigned block_sum_u(unsigned v, unsigned *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum_u(v);
-    __syncthreads();
+    sync_nt<NT>();
     if (lane == 0) red[w] = v;
-    __syncthreads();
+    sync_nt<NT>();
     unsigned t = lane < NT / 32 ? red[lane] : 0u;
     return warp_sum_u(t);
 }
@@ -208,9 +238,9 @@ __device__ __forceinline__ MaxSum warp_ms(MaxSum v, float c2) {
 template <int NT> __device__ __forceinline__ MaxSum block_ms(MaxSum v, float c2, float2 *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_ms(v, c2);
-    __syncthreads();
+    sync_nt<NT>();
     if (lane == 0) red[w] = make_float2(v.m, v.s);
-    __syncthreads();
+    sync_nt<NT>();
     MaxSum t = lane < NT / 32 ? MaxSum{red[lane].x, red[lane].y} : MaxSum{-INFINITY, 0.0f};
     return warp_ms(t, c2);
 }

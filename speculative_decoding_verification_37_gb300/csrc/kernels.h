@@ -66,18 +66,9 @@ struct ArgmaxParams {
 };
 
 constexpr int kTopKFastMax = 128;  // top_k served by the row-per-block path
-constexpr int kKeptRowMax = 256;   // kept entries of one row the top-k path publishes
-
-// One row's kept set on the top-k path, published for its position's
-// deciding block (16-byte words, read with two vector loads).
-struct alignas(16) TopkRow {
-    unsigned kn;      // kept entries, token order, in the row's entry array
-    unsigned th;      // order key of the threshold: every kept logit's key is >= it
-    float m;          // largest kept logit (-inf: no finite logit)
-    float s_hi, s_lo; // sum over the kept set of exp((l - m)/T), double-float
-    unsigned flags;   // 1: the kept set did not fit (the position takes the exact path)
-    unsigned pad[2];
-};
+constexpr int kKeptRowMax = 256;   // kept entries of one row a position can hold
+constexpr int kTopKGroups = 4;     // groups per thread the top-k pass hands on
+constexpr int kTopKThreads = 256;  // threads of a top-k pass block
 
 // Full-vocabulary persistent path (verify_full.cu): a request's draw record
 // and one (request, slice) result of a draw round.
@@ -111,11 +102,11 @@ struct SampleParams {
     unsigned *status, *counters;
     unsigned *rejword;  // [B] earliest rejection seen: gamma - k + 1, 0 = none
     PosRec *recs;       // [B*(gamma+1)]
-    // top-k path: per (position, row) the kept set published for the
-    // position's deciding block, and one arrival counter per position
-    TopkRow *rkrow;      // [B*(gamma+1)][2]
-    uint2 *rkent;        // [B*(gamma+1)][2][kKeptRowMax] (order key, token id), token order
-    unsigned *rkcnt;     // [B*(gamma+1)], zero between calls
+    // top-k path: per (position, row) slot pos*2 + r, what the pass hands
+    // the decision: each thread's maximum (order key) and its four largest
+    // groups (key prefix << 16 | chunk), thread-minor
+    uint32_t *rkmax;     // [B*(gamma+1)*2][kTopKThreads]
+    uint32_t *rkgrp;     // [B*(gamma+1)*2][kTopKGroups][kTopKThreads]
     // full-vocabulary persistent path, c = slices of full_row_bytes()
     float2 *fpart;               // [B*(gamma+1)][2][c] (max, sum) per slice
     float2 *fxd;                 // [B*(gamma+1)] target and draft logit at the draft token
@@ -194,7 +185,7 @@ long long full_idle_limit();  // the default of SampleParams::idle_limit
 float full_ex2_bound();       // the hardware exponential's relative error the certified draw assumes
 int full_row_bytes();   // one row's slice of the full-vocabulary path
 int full_max_slices();  // slices per row it supports
-int topk_row_bytes();  // a top-k slice body per row must fit this
+int topk_row_bytes();   // bytes of a row per streamed chunk on the top-k path
 struct CommitGeom {
     int ppu, upp, groups;
 };

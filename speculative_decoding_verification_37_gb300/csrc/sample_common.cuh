@@ -220,9 +220,9 @@ __device__ __forceinline__ void block_dd_sum2(dd &a, dd &b, float4 *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     a = warp_dd_sum(a);
     b = warp_dd_sum(b);
-    __syncthreads();
+    sync_nt<kNT>();
     if (lane == 0) red[w] = make_float4(a.hi, a.lo, b.hi, b.lo);
-    __syncthreads();
+    sync_nt<kNT>();
     dd ta{0.0f, 0.0f}, tb{0.0f, 0.0f};
     for (int i = 0; i < NT / 32; ++i) {
         ta = dd_add(ta, dd{red[i].x, red[i].y});
@@ -241,7 +241,7 @@ template <int NT, typename W>
 __device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBase &sb) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) { sb.found = INT_MAX; sb.lastpos = -1; }
-    __syncthreads();
+    sync_nt<kNT>();
     for (int base = lo; base < hi; base += NT * kScanE) {
         const int i0 = base + tid * kScanE;
         dd w[kScanE];
@@ -261,9 +261,9 @@ __device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBas
             const dd y{__shfl_up_sync(kFull, incl.hi, o), __shfl_up_sync(kFull, incl.lo, o)};
             if (lane >= o) incl = dd_add(y, incl);
         }
-        __syncthreads();
+        sync_nt<kNT>();
         if (lane == 31) sb.redd[wid] = make_float4(incl.hi, incl.lo, 0.0f, 0.0f);
-        __syncthreads();
+        sync_nt<kNT>();
         dd wpre{0.0f, 0.0f}, tile{0.0f, 0.0f};
         for (int q = 0; q < NT / 32; ++q) {
             const dd x{sb.redd[q].x, sb.redd[q].y};
@@ -282,7 +282,7 @@ __device__ int dd_scan_slice(int lo, int hi, dd carry, dd t, W &&weight, SampBas
         }
         if (hit != INT_MAX) atomicMin(&sb.found, hit);
         if (lastp >= 0) atomicMax(&sb.lastpos, lastp);
-        __syncthreads();
+        sync_nt<kNT>();
         if (sb.found != INT_MAX) break;
         carry = dd_add(carry, tile);
     }
@@ -477,7 +477,7 @@ struct SoloEx {
     int c = 1, j = 0;
     __device__ void ready() {}
     template <class P> __device__ P *at(P *local, int) { return local; }
-    __device__ void sync() { __syncthreads(); }
+    __device__ void sync() { sync_nt<kNT>(); }
 };
 
 // ---------------------------------------------------------------------------
@@ -498,7 +498,7 @@ __device__ void greedy_position(const SampleParams &p, SampBase &sb, Ex &ex, int
     });
     am = warp_argmax(am);
     if (lane == 0) sb.redd[wid] = make_float4(am.v, __int_as_float(am.idx), 0.0f, 0.0f);
-    __syncthreads();
+    sync_nt<kNT>();
     ArgMax t{-INFINITY, -1};
     if (lane < kNW) t = ArgMax{sb.redd[lane].x, __float_as_int(sb.redd[lane].y)};
     t = warp_argmax(t);
@@ -546,7 +546,7 @@ __device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const 
         const int sh = nb > 8 ? nb - 8 : 0;
         const uint32_t dmask = (1u << (nb - sh)) - 1u;
         hist[tid] = 0.0;
-        __syncthreads();
+        sync_nt<kNT>();
         for_slice<T, 4>(row, lo, hi, tid, kNT, [&](float x, int) {
             const uint32_t key = fkey(x) >> KS;
             if (x > -INFINITY && key >= th && (nb == KB || (key >> nb) == (prefix >> nb))) {
@@ -554,7 +554,7 @@ __device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const 
                 atomicAdd(&hist[(key >> sh) & dmask], (double)e.hi + (double)e.lo);
             }
         });
-        __syncthreads();
+        sync_nt<kNT>();
         ex.ready();
         ex.at(all, 0)[j * 256 + tid] = hist[tid];
         ex.sync();
@@ -570,7 +570,7 @@ __device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const 
                 if (lane >= o) incl += y;
             }
             if (lane == 31) sb.redD[wid] = incl;
-            __syncthreads();
+            sync_nt<kNT>();
             double pre = 0.0, tot = 0.0;
             for (int w = 0; w < kNW; ++w) {
                 pre += w < wid ? sb.redD[w] : 0.0;
@@ -580,7 +580,7 @@ __device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const 
             const double cum = above + pre + incl;
             const bool hit = v > 0.0 && cum >= target && cum - v < target;
             if (tid == 0) sb.nuc_found = 0;
-            __syncthreads();
+            sync_nt<kNT>();
             if (hit) {
                 sb.nuc_found = 1;
                 for (int r = 0; r < c; ++r) {
@@ -588,13 +588,13 @@ __device__ uint32_t nucleus_key(Ex &ex, SampBase &sb, unsigned char *dsm, const 
                     *ex.at(&sb.nuc_above, r) = cum - v;
                 }
             }
-            __syncthreads();
+            sync_nt<kNT>();
             if (!sb.nuc_found) {
                 // rounding left the mass below top_p: the smallest nonempty digit
                 unsigned lastd = v > 0.0 ? (unsigned)tid + 1u : 0u;
                 lastd = __reduce_max_sync(kFull, lastd);
                 if (lane == 0) sb.redD[wid] = (double)lastd;
-                __syncthreads();
+                sync_nt<kNT>();
                 unsigned best = 0u;
                 for (int w = 0; w < kNW; ++w) best = max(best, (unsigned)sb.redD[w]);
                 if (best > 0u && tid == (int)best - 1)
@@ -643,7 +643,7 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
     }
     if (p.per_request) {  // this request's 1/T for the double-float exponential
         if (tid == 0) sb.K.it = cfg.it;
-        __syncthreads();
+        sync_nt<kNT>();
     }
     const bool has_draft = k < cfg.gamma;
     const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)(b * (g + 1) + k) * p.tstride;
@@ -792,7 +792,7 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
             return (!MASK || (fkey(y) >> KS) >= th_q) ? dd_expw(y, mq, K) : dd{0.0f, 0.0f};
         };
         if (tid == 0) sb.namb = 0;
-        __syncthreads();
+        sync_nt<kNT>();
         dd sp{0.0f, 0.0f}, sq{0.0f, 0.0f}, pp{0.0f, 0.0f}, pq{0.0f, 0.0f};
         if (has_draft) {
             const float rho = Mp.s / Mq.s;  // fp32 estimate of S_p / S_q
@@ -866,7 +866,7 @@ __device__ void masked_position(const SampleParams &p, SampBase &sb, unsigned ch
             dd unused{0.0f, 0.0f};
             block_dd_sum2<kNT>(zw, unused, sb.redd);
             if (!any_ovf) zw = dd_add(zw, dd_add(dd_mul(pp, isp), dd_neg(dd_mul(pq, isq))));
-            __syncthreads();
+            sync_nt<kNT>();
             if (tid < c) *ex.at(&sb.dsum2[j], tid) = make_float4(zw.hi, zw.lo, 0.0f, 0.0f);
             ex.sync();
             dd Zw{0.0f, 0.0f};

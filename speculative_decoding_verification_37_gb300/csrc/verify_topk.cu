@@ -1,5 +1,5 @@
-// Sampled chain verification with top-k (k <= 128) on sm_103a: one block per
-// logits row, in one kernel.
+// Sampled chain verification with top-k (k <= 128) on sm_103a: a pass over
+// the logits, then one block per position.
 //
 // The transform ("KV Cache 优化（四）：Speculative Decoding 投机解码" §4) keeps
 // every logit >= the row's k-th largest, so after one pass over a row only a
@@ -7,37 +7,39 @@
 // the draw ("10.6 投机解码：为什么“先猜后验”能加速" §10.6.1) then work on the
 // two kept sets of a position.
 //
-// chain_topk_row_kernel: a persistent grid of a few blocks per SM; block i
-// takes rows i, i + grid, ... (target row (b,k) and draft row (b,k) of each
-// position are neighbours, positions in order).  For its row a block
-//  1. streams the 16-byte-aligned body through a ring of shared-memory stages
-//     (thread 0 issues one cp.async.bulk per 16 KiB chunk with an evict-first
-//     L2 policy, completing on the stage's mbarrier, waits bounded); the
-//     scalar head and tail come from plain loads;
-//  2. keeps theta, a lower bound of the row's k-th largest logit: from the
-//     first chunk, the k-th largest of the threads' maxima (each is a logit,
-//     so at least k logits reach it); later, the k-th largest of the listed
-//     candidates.  Each thread takes the largest element of each of its
-//     16-byte vectors (packed bf16x2 maxima); only vectors reaching theta
-//     have their elements listed (order key, token id) in a shared-memory
-//     candidate buffer.  One block barrier per chunk gives every warp its
-//     offset; when the buffer passes a soft limit one warp compacts it to
-//     the entries >= its k-th largest (theta rises); if a chunk would not fit,
-//     the chunk's own k-th largest (a block radix search over its elements in
-//     registers) raises theta first;
-//  3. takes the exact threshold (the k-th largest candidate), the kept set in
-//     token order, its maximum and double-float normaliser (and the nucleus
-//     when top_p is set), and publishes them to the workspace;
-//  4. arrives on its position's counter: the block that arrives second (the
-//     bonus position has one row) loads the other row's kept set and decides
-//     the position with one warp: a_k = min(1, p(d)/q(d)), the residual mass
-//     over the target's kept set (q looked up in the draft's), and the draw
-//     where this position decides the token, by a double-float warp scan in
-//     token order; finish() records it and the last position of a request
-//     writes the request's outputs.
-// A row whose candidates do not fit (hundreds of logits tied at the
-// threshold) sends its position to the exact masked computation over both
-// rows in the deciding block, the nucleus included (slow, exact, rare).
+// chain_topk_pass_kernel: a persistent grid of four blocks per SM; block i
+// takes rows i, i + grid, ...  For its row a block streams the 16-byte-aligned
+// body through a ring of shared-memory stages (thread 0 issues one
+// cp.async.bulk per 16 KiB chunk with an evict-first L2 policy, completing on
+// the stage's mbarrier, waits bounded).  Per chunk a thread only takes the
+// maximum of its four 16-byte vectors (packed bf16x2 maxima): a "group" is
+// (chunk, thread).  It keeps its maximum over the row (the scalar head and
+// tail included) and its four largest groups (16-bit key prefix and chunk),
+// and writes them to the workspace at the row's end: the pass streams at the
+// memory's pace, with nothing else to wait for.
+//
+// chain_topk_decide_kernel: one block per position, launched as a
+// programmatic dependent of the pass (its launch overlaps the pass's tail;
+// it waits for the pass's results before reading them).  Per row:
+//  1. theta = the k-th largest of the threads' maxima (each is a logit, so at
+//     least k logits reach it: a lower bound of the row's k-th largest).
+//     Only groups whose maximum reaches theta's prefix can hold a kept
+//     logit, and each thread's such groups are among its four largest unless
+//     the fourth qualifies too (ties: then the position takes the exact
+//     path).  Each thread reloads its candidate groups (both rows' loads in
+//     flight together) and lists their elements >= theta, and the head and
+//     tail scalars >= theta, (order key, token id) in a shared buffer;
+//  2. the kept set: an entry is kept iff fewer than k listed entries are
+//     larger, i.e. exactly the logits >= the k-th largest; then token order,
+//     the maximum and the double-float normaliser (and the nucleus when
+//     top_p is set);
+// then a_k = min(1, p(d)/q(d)), the residual mass over the target's kept set
+// (q looked up in the draft's), and the draw where this position decides the
+// token, by a double-float scan in token order; finish() records it and the
+// last position of a request writes the request's outputs.  A position whose
+// candidates do not fit (many logits tied at the threshold) takes the exact
+// masked computation over both rows instead, the nucleus included (slow,
+// exact, rare).
 #include "sample_common.cuh"
 
 namespace specv {
@@ -45,20 +47,19 @@ namespace specv {
 constexpr int kRkCH = 16384;              // bytes of a row's body per ring stage
 constexpr int kRkNST = 3;                 // ring stages
 constexpr int kRkCap = 512;               // candidate entries a row can hold
-constexpr int kRkSoft = 320;              // more than this after a chunk: compact
-constexpr int kRkBlocksPerSM = 4;
+constexpr int kRkBlocksPerSM = 4;         // pass blocks per SM
 constexpr int kRkVec = kRkCH / 16 / kNT;  // 16-byte vectors per thread and chunk
 static_assert(kRkVec * 16 * kNT == kRkCH, "a chunk is whole vectors per thread");
 static_assert(kRkVec * 8 <= 32, "a thread's hit bits fit one word");
+static_assert(kKeptMax == kNT, "one kept-set slot per thread");
+static_assert(kTopKThreads == kNT && kTopKGroups == 4, "the workspace layout of the pass's results");
 
 struct RkRing {
     alignas(128) unsigned char buf[kRkNST][kRkCH];
 };
 using RkFallbackRing = Ring<8192, 2, 2>;  // the exact masked path's ring
-constexpr size_t kRkRingBytes = sizeof(RkRing) > sizeof(RkFallbackRing) ? sizeof(RkRing) : sizeof(RkFallbackRing);
-constexpr size_t kRkDyn = kRkRingBytes + kRkCap * sizeof(uint2);
 
-// Decision-time arrays, in the ring's memory (no copy is in flight then).
+// The decision's arrays (dynamic shared memory of a decide block).
 struct RkDecide {
     uint2 kept[2][kKeptMax];     // target / draft kept set, token order
     float2 wp[2][kKeptMax];      // per kept target entry: p (or the bonus term) and residual weight
@@ -68,9 +69,12 @@ struct RkDecide {
     float m[2];
     float2 S[2];
 };
-static_assert(sizeof(RkDecide) <= sizeof(RkRing), "decision arrays fit the ring");
-
-constexpr unsigned RK_OVERFLOW = 1u;  // the row's candidates or kept set did not fit
+constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
+// a decide block's dynamic shared memory: the decision arrays and both rows'
+// candidate buffers, or the exact path's ring
+constexpr size_t kRkCandOff = (sizeof(RkDecide) + 15) / 16 * 16;
+constexpr size_t kRkDecideDyn =
+    (cmax(sizeof(RkFallbackRing), kRkCandOff + 2 * kRkCap * sizeof(uint2)) + 127) / 128 * 128;
 
 int topk_row_bytes() { return kRkCH; }
 
@@ -87,6 +91,30 @@ __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
 }
 template <> __device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4 &v) {
     const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+    return fmaxf(__low2float(a), __high2float(a));
+}
+
+// a 16-byte vector of -inf
+template <typename T> __device__ __forceinline__ uint4 vec_neg_inf();
+template <> __device__ __forceinline__ uint4 vec_neg_inf<float>() {
+    return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+}
+template <> __device__ __forceinline__ uint4 vec_neg_inf<__nv_bfloat16>() {
+    return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+}
+// largest element of N vectors (bf16: packed maxima, one conversion)
+template <typename T, int N> __device__ __forceinline__ float vecs_max(const uint4 (&v)[N]);
+template <> __device__ __forceinline__ float vecs_max<float, kRkVec>(const uint4 (&v)[kRkVec]) {
+    float m = vec_max<float>(v[0]);
+#pragma unroll
+    for (int i = 1; i < kRkVec; ++i) m = fmaxf(m, vec_max<float>(v[i]));
+    return m;
+}
+template <> __device__ __forceinline__ float vecs_max<__nv_bfloat16, kRkVec>(const uint4 (&v)[kRkVec]) {
+    __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v[0].x), as_bf2(v[0].y)), __hmax2(as_bf2(v[0].z), as_bf2(v[0].w)));
+#pragma unroll
+    for (int i = 1; i < kRkVec; ++i)
+        a = __hmax2(a, __hmax2(__hmax2(as_bf2(v[i].x), as_bf2(v[i].y)), __hmax2(as_bf2(v[i].z), as_bf2(v[i].w))));
     return fmaxf(__low2float(a), __high2float(a));
 }
 
@@ -136,54 +164,6 @@ __device__ __forceinline__ dd warp_dd_excl_scan(dd v) {
 template <typename T> __device__ __forceinline__ float lowest_finite();
 template <> __device__ __forceinline__ float lowest_finite<float>() { return -3.40282347e38f; }
 template <> __device__ __forceinline__ float lowest_finite<__nv_bfloat16>() { return __uint_as_float(0xff7f0000u); }
-
-// The K-th largest order key among the finite elements the block holds in
-// registers (each thread: its vectors v[i] whose slot is < nv, and in the
-// first chunk its head/tail scalars), by a 2-bit radix descent with block
-// counts; 0 if fewer than K.  Every thread gets it.  All threads call it.
-template <typename T>
-__device__ __forceinline__ uint32_t block_kth_chunk(const uint4 *v, int nv, float xh, float xt, unsigned K,
-                                    unsigned (*red)[3][kNW]) {
-    constexpr int VEC = Elem<T>::VEC;
-    constexpr int KB = Elem<T>::KEY_BITS;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    uint32_t res = 0u;
-    auto cnt = [&](float x, uint32_t c) -> unsigned { return (x > -INFINITY && kkey<T>(x) >= c) ? 1u : 0u; };
-    int par = 0;
-    for (int bit = KB - 2; bit >= 0; bit -= 2, par ^= 1) {
-        const uint32_t c1 = res | (1u << bit), c2 = res | (2u << bit), c3 = res | (3u << bit);
-        unsigned n1 = cnt(xh, c1) + cnt(xt, c1), n2 = cnt(xh, c2) + cnt(xt, c2), n3 = cnt(xh, c3) + cnt(xt, c3);
-#pragma unroll
-        for (int i = 0; i < kRkVec; ++i) {
-            if (tid + i * kNT >= nv) continue;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float x = vec_elem<T>(v[i], e);
-                n1 += cnt(x, c1);
-                n2 += cnt(x, c2);
-                n3 += cnt(x, c3);
-            }
-        }
-        n1 = __reduce_add_sync(kFull, n1);
-        n2 = __reduce_add_sync(kFull, n2);
-        n3 = __reduce_add_sync(kFull, n3);
-        if (lane == 0) {
-            red[par][0][wid] = n1;
-            red[par][1][wid] = n2;
-            red[par][2][wid] = n3;
-        }
-        __syncthreads();
-        unsigned t1 = 0, t2 = 0, t3 = 0;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-            t1 += red[par][0][w];
-            t2 += red[par][1][w];
-            t3 += red[par][2][w];
-        }
-        res |= (t3 >= K ? 3u : t2 >= K ? 2u : t1 >= K ? 1u : 0u) << bit;
-    }
-    return res;
-}
 
 // ---------------------------------------------------------------------------
 // Block-wide helpers.  Everything after a row's stream runs on the whole
@@ -241,6 +221,59 @@ __device__ uint32_t block_kth(uint32_t k0, uint32_t k1, unsigned K, RkRed &rd) {
         if (n >= K) res = c;
     }
     return res;
+}
+
+// The K-th largest of two key sets at once (k0: row 0's key of this thread,
+// k1: row 1's; 0 = no key): per set the largest r such that at least K keys
+// are >= r, 0 if the set has fewer than K keys.  Two bits per step, counted
+// with warp ballots and one block barrier (counts double-buffered by step
+// parity).  Every thread calls it and gets both results.
+struct RkPairRed {
+    unsigned c[2][kNW][8];
+};
+template <int KB>
+__device__ void block_kth_pair(uint32_t k0, uint32_t k1, unsigned K, RkPairRed &pr, uint32_t &r0, uint32_t &r1) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // step -1: how many keys each set has
+    unsigned h0 = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u)), h1 = (unsigned)__popc(__ballot_sync(kFull, k1 != 0u));
+    if (lane == 0) {
+        pr.c[1][wid][0] = h0;
+        pr.c[1][wid][1] = h1;
+    }
+    __syncthreads();
+    h0 = h1 = 0u;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+        h0 += pr.c[1][w][0];
+        h1 += pr.c[1][w][1];
+    }
+    uint32_t a = 0u, b = 0u;  // the answers' bits fixed so far
+    int par = 0;
+#pragma unroll 1
+    for (int bit = KB - 2; bit >= 0; bit -= 2, par ^= 1) {
+        unsigned n[6];
+#pragma unroll
+        for (int d = 1; d <= 3; ++d) {
+            n[d - 1] = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u && k0 >= (a | ((uint32_t)d << bit))));
+            n[d + 2] = (unsigned)__popc(__ballot_sync(kFull, k1 != 0u && k1 >= (b | ((uint32_t)d << bit))));
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < 6; ++j) pr.c[par][wid][j] = n[j];
+        __syncthreads();
+        // lane j < 6 sums count j over the warps; every lane takes the six sums
+        unsigned mine = 0u;
+        if (lane < 6)
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) mine += pr.c[par][w][lane];
+        unsigned t[6];
+#pragma unroll
+        for (int j = 0; j < 6; ++j) t[j] = __shfl_sync(kFull, mine, j);
+        a |= (t[2] >= K ? 3u : t[1] >= K ? 2u : t[0] >= K ? 1u : 0u) << bit;
+        b |= (t[5] >= K ? 3u : t[4] >= K ? 2u : t[3] >= K ? 1u : 0u) << bit;
+    }
+    r0 = h0 >= K ? a : 0u;
+    r1 = h1 >= K ? b : 0u;
 }
 
 // Writes the flagged entries (up to two per thread) to dst in thread order,
@@ -355,6 +388,14 @@ __device__ __noinline__ void row_top_p(uint2 *kept, int &kn, uint32_t &th, float
     S = warp_dd_sum(S);
 }
 
+// A position's inputs the deciding block needs: its draft token, its two
+// uniforms and the request's rejection word, read before the decision.
+struct RkInputs {
+    int d;
+    float u_k, u_f;
+    unsigned rej;
+};
+
 // The outcome of position k of request b from the two kept sets (token
 // order, one entry per thread) and their row statistics: acceptance, the
 // residual mass, and the draw where this position decides the emitted
@@ -362,20 +403,13 @@ __device__ __noinline__ void row_top_p(uint2 *kept, int &kn, uint32_t &th, float
 // result is the same in every thread.
 template <typename T>
 __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int k, RkDecide &D, const DdExpTables &EK,
-                                              RkRed &rd, unsigned *s_rej) {
+                                              RkRed &rd, float4 *red4, const RkInputs &in) {
     const int tid = threadIdx.x;
     const int g = p.gamma;
     const bool has_draft = k < g;
-    const int pos = b * (g + 1) + k;
-    const T *trow = reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride;
-    const T *drow = has_draft ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride : nullptr;
-    const int d = has_draft ? p.tokens[(int64_t)b * g + k] : 0;
+    const int d = in.d;
     const bool bad_tok = has_draft && (d < 0 || d >= p.V);
-    const float l_d = (has_draft && !bad_tok) ? ld_elem(trow, d) : 0.0f;
-    const float g_d = (has_draft && !bad_tok) ? ld_elem(drow, d) : 0.0f;
-    const float u_k = has_draft ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
-    const float u_f = p.unif[(int64_t)b * (g + 1) + g];
-    if (tid == 0) *s_rej = *((volatile unsigned *)&p.rejword[b]);  // one read, shared by the block
+    const float u_k = in.u_k, u_f = in.u_f;
     const uint2 *Kp = D.kept[0], *Kq = D.kept[1];
     const int np = (int)D.kn[0], nq = has_draft ? (int)D.kn[1] : 0;
     const float mp = D.m[0], mq = has_draft ? D.m[1] : 0.0f;
@@ -384,15 +418,24 @@ __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int 
     Outcome o{1.0f, 0.0f, -1, 0u};
     const bool bad_row = mp == -INFINITY || (has_draft && mq == -INFINITY);
     o.info = (bad_tok ? REC_BAD_INPUT : 0u) | (bad_row ? REC_BAD_ROW : 0u);
-    __syncthreads();
-    const unsigned rej = *s_rej;
+    const unsigned rej = in.rej;
     if (bad_tok || bad_row) return o;
     const dd isp = dd_recip(sp);
     const dd isq = has_draft ? dd_recip(sq) : dd{0.0f, 0.0f};
     bool accept = false;
     if (has_draft) {
-        const dd pd = kkey<T>(l_d) >= D.th[0] ? dd_mul(dd_expw(l_d, mp, EK), isp) : dd{0.0f, 0.0f};
-        const dd qd = kkey<T>(g_d) >= D.th[1] ? dd_mul(dd_expw(g_d, mq, EK), isq) : dd{0.0f, 0.0f};
+        // p(d), q(d): d's entry in each kept set (token order), 0 when d is not kept
+        auto find = [&](const uint2 *kp, int n) -> int {
+            int lo = 0, hi = n;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (kp[mid].y < (uint32_t)d) lo = mid + 1; else hi = mid;
+            }
+            return lo < n && kp[lo].y == (uint32_t)d ? lo : -1;
+        };
+        const int ip = find(Kp, np), iq = find(Kq, nq);
+        const dd pd = ip >= 0 ? dd_mul(dd_expw(key_value<T>(Kp[ip].x), mp, EK), isp) : dd{0.0f, 0.0f};
+        const dd qd = iq >= 0 ? dd_mul(dd_expw(key_value<T>(Kq[iq].x), mq, EK), isq) : dd{0.0f, 0.0f};
         float a;
         if (dd_pos(qd)) {
             const dd ratio = dd_mul(pd, dd_recip(qd));
@@ -425,9 +468,10 @@ __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int 
         }
     }
     dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
-    if (has_draft) {
-        zw = block_dd_sum(w, rd);
-        zp = block_dd_sum(pi, rd);
+    if (has_draft) {  // both sums in one block reduction
+        zw = w;
+        zp = pi;
+        block_dd_sum2<kNT>(zw, zp, red4);
         o.z = dd_to_f(zw);
     }
     const bool earlier = rej > (unsigned)(g - k + 1);
@@ -441,8 +485,22 @@ __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int 
         const dd t = dd_mul_f(total, u_f);
         const dd cum = block_dd_incl_scan(wt, rd);
         const bool pos_w = tid < np && dd_pos(wt);
-        const unsigned hit = block_min_u((pos_w && dd_gt(cum, t)) ? (unsigned)tid : 0xffffffffu, rd.u[0]);
-        const unsigned lastp = block_max_u(pos_w ? (unsigned)tid + 1u : 0u, rd.u[1]);
+        // the first entry past t, and the last with weight (when rounding
+        // leaves the total short of t), in one exchange
+        const int lane = tid & 31, wid = tid >> 5;
+        const unsigned hw = __reduce_min_sync(kFull, (pos_w && dd_gt(cum, t)) ? (unsigned)tid : 0xffffffffu);
+        const unsigned lw = __reduce_max_sync(kFull, pos_w ? (unsigned)tid + 1u : 0u);
+        if (lane == 0) {
+            rd.u[0][wid] = hw;
+            rd.u[1][wid] = lw;
+        }
+        __syncthreads();
+        unsigned hit = 0xffffffffu, lastp = 0u;
+#pragma unroll
+        for (int x = 0; x < kNW; ++x) {
+            hit = min(hit, rd.u[0][x]);
+            lastp = max(lastp, rd.u[1][x]);
+        }
         const int sel = hit != 0xffffffffu ? (int)hit : (int)lastp - 1;
         o.token = sel >= 0 ? (int)Kp[sel].y : -1;
     }
@@ -457,33 +515,23 @@ __device__ __noinline__ void rk_exact_position(const SampleParams &p, SampBase &
     masked_position<T, true, SoloEx, RkFallbackRing>(p, sb, dsm, solo, k, b, 0, p.V);
 }
 
+
+// The pass: every row's thread maxima and four largest groups.
 template <typename T>
-__global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_row_kernel(SampleParams p) {
-    constexpr int VEC = Elem<T>::VEC;
-    constexpr int ECH = kRkCH / (int)sizeof(T);  // elements per chunk
-    __shared__ SampBase sb;
+__global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_pass_kernel(SampleParams p) {
+    constexpr int KB = Elem<T>::KEY_BITS;
     __shared__ __align__(8) unsigned long long full[kRkNST];
-    __shared__ unsigned s_wcnt[3][kNW];
-    __shared__ unsigned s_red[2][3][kNW];
-    __shared__ RkRed rd;
-    __shared__ unsigned s_last, s_rej;
     extern __shared__ __align__(128) unsigned char dsm[];
     RkRing &R = *reinterpret_cast<RkRing *>(dsm);
-    RkDecide &D = *reinterpret_cast<RkDecide *>(dsm);
-    uint2 *cand = reinterpret_cast<uint2 *>(dsm + kRkRingBytes);
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const unsigned lt = lanemask_lt();
-    const unsigned K = (unsigned)p.top_k;
+    const int tid = threadIdx.x;
     const int g = p.gamma, B = p.B;
     const int nrows = B * (2 * g + 1);
-    const bool nucleus = p.top_p > 0.0f && p.top_p < 1.0f;
-    load_exp_tables(p, sb);
     if (tid == 0) {
         for (int s = 0; s < kRkNST; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
     __syncthreads();
-    const DdExpTables &EK = sb.K;
+    pdl_launch_dependents();  // the decision blocks may be scheduled; they wait for this grid's end
     const uint64_t pol = l2_evict_first();
     unsigned seq = 0;  // chunks this block has consumed: the ring stage and phase of the next
 
@@ -518,274 +566,439 @@ __global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_row_kernel(Sam
         if (tid == 0)
             for (; issued < kRkNST && issued < nch; ++issued) issue(issued);
         const int nhead = sp.body0 - sp.head0, ntail = sp.hi - sp.tail0;
-        const float xh = tid < nhead ? ld_elem(row, sp.head0 + tid) : -INFINITY;
-        const float xt = tid < ntail ? ld_elem(row, sp.tail0 + tid) : -INFINITY;
-
-        uint32_t theta = 0u;  // order key of the running lower bound of the k-th largest
-        int count = 0;        // candidates in the buffer
-        bool ovf = false, tmo = false;
+        float tmax = fmaxf(tid < nhead ? ld_elem(row, sp.head0 + tid) : -INFINITY,
+                           tid < ntail ? ld_elem(row, sp.tail0 + tid) : -INFINITY);
+        // the four largest groups, (key prefix << 16 | chunk), descending; 0 = none
+        uint32_t t4[4] = {0u, 0u, 0u, 0u};
+        bool tmo = false;
         int failed_at = -1;
-        const int nwin = nch > 0 ? nch : 1;
-        for (int w = 0; w < nwin; ++w) {
+        for (int w = 0; w < nch; ++w) {
             const unsigned gq = seq + (unsigned)w;
             const int s = (int)(gq % kRkNST);
+            if (!mbar_wait_bounded(&full[s], (gq / kRkNST) & 1u)) tmo = true;
+            const int nv = (int)(min((uint32_t)kRkCH, body - (uint32_t)w * kRkCH) / 16u);
+            const uint4 *st = reinterpret_cast<const uint4 *>(R.buf[s]);
             uint4 v[kRkVec];
-            int nv = 0;
-            if (w < nch) {
-                if (!mbar_wait_bounded(&full[s], (gq / kRkNST) & 1u)) tmo = true;
-                nv = (int)(min((uint32_t)kRkCH, body - (uint32_t)w * kRkCH) / 16u);
-                const uint4 *st = reinterpret_cast<const uint4 *>(R.buf[s]);
-#pragma unroll
-                for (int i = 0; i < kRkVec; ++i) {
-                    const int qv = tid + i * kNT;
-                    v[i] = qv < nv ? st[qv] : make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            float vm[kRkVec];
-            float tm = w == 0 ? fmaxf(xh, xt) : -INFINITY;
 #pragma unroll
             for (int i = 0; i < kRkVec; ++i) {
-                vm[i] = tid + i * kNT < nv ? vec_max<T>(v[i]) : -INFINITY;
-                tm = fmaxf(tm, vm[i]);
+                const int qv = tid + i * kNT;
+                v[i] = qv < nv ? st[qv] : vec_neg_inf<T>();
             }
-            const int vbase = sp.body0 + w * ECH;  // element index of the chunk's first element
-            if (w == 0)  // the k-th largest thread maximum: at least k logits reach it
-                theta = block_kth<false>(tm > -INFINITY ? kkey<T>(tm) : 0u, 0u, K, rd);
-            // the listed elements: hit bits (VEC per vector) and scalar flags
-            uint32_t hm = 0u;
-            bool hh = false, ht = false;
-            auto tally = [&]() -> unsigned {
-                hm = 0u;
-                hh = ht = false;
-                if (ovf) return 0u;
-                const float tf = fmaxf(key_value<T>(theta), lowest_finite<T>());
-                if (tm >= tf) {
+            const float tm = vecs_max<T, kRkVec>(v);
+            tmax = fmaxf(tmax, tm);
+            uint32_t x = tm > -INFINITY ? ((kkey<T>(tm) >> (KB - 16)) << 16) | (uint32_t)w : 0u;
 #pragma unroll
-                    for (int i = 0; i < kRkVec; ++i)
-                        if (vm[i] >= tf) hm |= vec_ge_mask<T>(v[i], tf) << (VEC * i);
-                    hh = xh >= tf && w == 0;
-                    ht = xt >= tf && w == 0;
-                }
-                return (unsigned)__popc(hm) + (hh ? 1u : 0u) + (ht ? 1u : 0u);
-            };
-            unsigned n = tally();
-            unsigned wt = __reduce_add_sync(kFull, n);
-            if (lane == 0) s_wcnt[w & 1][wid] = wt;
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t hi = max(t4[j], x);
+                x = min(t4[j], x);
+                t4[j] = hi;
+            }
             if (__syncthreads_or(tmo)) {  // block-uniform: a chunk did not arrive
                 failed_at = w;
                 break;
             }
             // every thread holds its share of the chunk: refill the stage
             if (tid == 0 && issued < nch) issue(issued++);
-            unsigned tot = 0u, before = 0u;
-#pragma unroll
-            for (int x = 0; x < kNW; ++x) {
-                const unsigned cw = s_wcnt[w & 1][x];
-                tot += cw;
-                before += x < wid ? cw : 0u;
-            }
-            if (count + (int)tot > kRkCap) {
-                // the chunk does not fit: raise theta by the chunk's own k-th
-                // largest element and the buffer's, compact, count again
-                uint32_t th = block_kth_chunk<T>(v, nv, w == 0 ? xh : -INFINITY, w == 0 ? xt : -INFINITY, K, s_red);
-                th = max(th, theta);
-                const uint2 e0 = tid < count ? cand[tid] : make_uint2(0u, 0u);
-                const uint2 e1 = tid + kNT < count ? cand[tid + kNT] : make_uint2(0u, 0u);
-                if ((unsigned)count >= K) th = max(th, block_kth<true>(e0.x, e1.x, K, rd));
-                count = block_compact2(cand, kRkCap, e0, e0.x != 0u && e0.x >= th, e1, e1.x != 0u && e1.x >= th, rd);
-                theta = th;
-                n = tally();
-                wt = __reduce_add_sync(kFull, n);
-                if (lane == 0) s_wcnt[2][wid] = wt;
-                __syncthreads();
-                tot = before = 0u;
-#pragma unroll
-                for (int x = 0; x < kNW; ++x) {
-                    const unsigned cw = s_wcnt[2][x];
-                    tot += cw;
-                    before += x < wid ? cw : 0u;
-                }
-                if (count + (int)tot > kRkCap) ovf = true;  // block-uniform
-            }
-            if (!ovf && wt > 0u) {
-                unsigned incl = n;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned y = __shfl_up_sync(kFull, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                unsigned at = (unsigned)count + before + incl - n;
-#pragma unroll
-                for (int i = 0; i < kRkVec; ++i) {
-                    uint32_t h = (hm >> (VEC * i)) & ((1u << VEC) - 1u);
-                    while (h) {
-                        const int e = __ffs(h) - 1;
-                        h &= h - 1u;
-                        cand[at++] = make_uint2(kkey<T>(vec_elem<T>(v[i], e)),
-                                                (uint32_t)(vbase + (tid + i * kNT) * VEC + e));
-                    }
-                }
-                if (hh) cand[at++] = make_uint2(kkey<T>(xh), (uint32_t)(sp.head0 + tid));
-                if (ht) cand[at++] = make_uint2(kkey<T>(xt), (uint32_t)(sp.tail0 + tid));
-            }
-            if (!ovf) count += (int)tot;
-            if (!ovf && count > kRkSoft) {  // block-uniform
-                __syncthreads();  // the chunk's entries are in the buffer
-                const uint2 e0 = tid < count ? cand[tid] : make_uint2(0u, 0u);
-                const uint2 e1 = tid + kNT < count ? cand[tid + kNT] : make_uint2(0u, 0u);
-                const uint32_t th = max(theta, block_kth<true>(e0.x, e1.x, K, rd));
-                count = block_compact2(cand, kRkCap, e0, e0.x != 0u && e0.x >= th, e1, e1.x != 0u && e1.x >= th, rd);
-                theta = th;
-            }
         }
         if (failed_at >= 0) {
             // A bulk copy did not complete in time: issue nothing more, wait
             // (bounded) for the copies already issued so that none lands in
             // shared memory after the block has moved on, flag the call and stop.
             if (tid == 0) {
+                bool drained = true;
                 for (int c = failed_at; c < issued; ++c) {
                     const unsigned gq = seq + (unsigned)c;
-                    for (int rep = 0; rep < 4; ++rep)
-                        if (mbar_wait_bounded(&full[gq % kRkNST], (gq / kRkNST) & 1u)) break;
+                    drained &= mbar_drain(&full[gq % kRkNST], (gq / kRkNST) & 1u);
                 }
                 atomicOr(p.status, SPEC_FLAG_TIMEOUT);
+                if (drained)
+                    for (int s = 0; s < kRkNST; ++s) mbar_inval(&full[s]);
             }
             return;
         }
         seq += (unsigned)nch;
-        __syncthreads();  // the last chunk's entries are in the buffer; the ring is idle
-
-        // ---- the row's kept set: the exact threshold, token order, statistics ----
-        const int mine = r;
-        {
-            uint32_t th = 0u;
-            int kn = 0;
-            if (!ovf) {
-                const uint2 e0 = tid < count ? cand[tid] : make_uint2(0u, 0u);
-                const uint2 e1 = tid + kNT < count ? cand[tid + kNT] : make_uint2(0u, 0u);
-                th = block_kth<true>(e0.x, e1.x, K, rd);  // 0 (keep all) with fewer than K candidates
-                kn = block_compact2(D.tmp, kKeptMax, e0, e0.x != 0u && e0.x >= th, e1, e1.x != 0u && e1.x >= th, rd);
-                if (kn > kKeptMax) ovf = true;  // block-uniform
-            }
-            float m = -INFINITY;
-            dd S{0.0f, 0.0f};
-            if (!ovf) {
-                uint2 e = make_uint2(0u, 0u);
-                if (tid < kn) {
-                    e = D.tmp[tid];
-                    int rank = 0;
-                    for (int y = 0; y < kn; ++y) rank += D.tmp[y].y < e.y;
-                    D.kept[mine][rank] = e;
-                }
-                const uint32_t mk = block_max_u(e.x, rd.u[0]);
-                m = kn > 0 ? key_value<T>(mk) : -INFINITY;
-                if (m != -INFINITY) {
-                    S = block_dd_sum(tid < kn ? dd_expw(key_value<T>(e.x), m, EK) : dd{0.0f, 0.0f}, rd);
-                    if (nucleus) {
-                        if (wid == 0) {
-                            row_top_p<T>(D.kept[mine], kn, th, m, S, p.top_p, D.tmp, D.prb, EK);
-                            if (lane == 0) {
-                                D.kn[mine] = (unsigned)kn;
-                                D.th[mine] = th;
-                                D.S[mine] = make_float2(S.hi, S.lo);
-                            }
-                        }
-                        __syncthreads();
-                        kn = (int)D.kn[mine];
-                        th = D.th[mine];
-                        S = dd{D.S[mine].x, D.S[mine].y};
-                    }
-                }
-            }
-            __syncthreads();  // every thread has read D.kn/th/S above
-            if (tid == 0) {
-                D.kn[mine] = (unsigned)kn;
-                D.th[mine] = th;
-                D.m[mine] = m;
-                D.S[mine] = make_float2(S.hi, S.lo);
-                D.flags[mine] = ovf ? RK_OVERFLOW : 0u;
-            }
-            if (k < g) {  // publish for the position's other block
-                const int64_t ri = (int64_t)pos * 2 + r;
-                if (tid == 0) {
-                    TopkRow h;
-                    h.kn = (unsigned)kn;
-                    h.th = th;
-                    h.m = m;
-                    h.s_hi = S.hi;
-                    h.s_lo = S.lo;
-                    h.flags = ovf ? RK_OVERFLOW : 0u;
-                    h.pad[0] = h.pad[1] = 0u;
-                    p.rkrow[ri] = h;
-                }
-                if (!ovf && tid < kn) p.rkent[ri * kKeptMax + tid] = D.kept[mine][tid];
-                __threadfence();
-            }
-        }
-        __syncthreads();
-        // ---- the position's decision, by the block that arrives last ----
-        if (tid == 0) {
-            unsigned last = 1u;
-            if (k < g) {
-                last = atomicAdd(p.rkcnt + pos, 1u) == 1u;
-                if (last) {
-                    p.rkcnt[pos] = 0u;  // left zeroed for the next call
-                    __threadfence();
-                }
-            }
-            s_last = last;
-        }
-        __syncthreads();
-        if (s_last) {
-            if (k < g) {
-                // the other row's kept set and statistics
-                const int64_t ri = (int64_t)pos * 2 + (1 - r);
-                const uint4 *hp = reinterpret_cast<const uint4 *>(p.rkrow + ri);
-                const uint4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1);
-                const unsigned okn = h0.x;
-                if (tid == 0) {
-                    D.kn[1 - r] = okn;
-                    D.th[1 - r] = h0.y;
-                    D.m[1 - r] = __uint_as_float(h0.z);
-                    D.S[1 - r] = make_float2(__uint_as_float(h0.w), __uint_as_float(h1.x));
-                    D.flags[1 - r] = h1.y;
-                }
-                if (!(h1.y & RK_OVERFLOW) && tid < (int)okn && tid < kKeptMax)
-                    D.kept[1 - r][tid] = __ldcg(p.rkent + ri * kKeptMax + tid);
-            }
-            __syncthreads();
-            const bool exact = ((D.flags[0] | (k < g ? D.flags[1] : 0u)) & RK_OVERFLOW) != 0u;  // block-uniform
-            if (exact) {
-                rk_exact_position<T>(p, sb, dsm, k, b);
-            } else {
-                const Outcome o = block_outcome<T>(p, b, k, D, EK, rd, &s_rej);
-                finish(p, b, k, o, sb);
-            }
-        }
-        __syncthreads();  // the ring's memory is free again for the next row
+        const int64_t slot = (int64_t)pos * 2 + r;
+        p.rkmax[slot * kNT + tid] = tmax > -INFINITY ? kkey<T>(tmax) : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p.rkgrp[(slot * 4 + j) * kNT + tid] = t4[j];
     }
     if (tid == 0)
         for (int s = 0; s < kRkNST; ++s) mbar_inval(&full[s]);
 }
 
+// One row of a position, as the decide block sees it.
 template <typename T>
-static cudaError_t launch_rows(const SampleParams &p, int sms, cudaStream_t s) {
-    static std::atomic<unsigned long long> done{0};
-    cudaError_t e = ensure_smem_attr(chain_topk_row_kernel<T>, (int)kRkDyn, done);
+struct RkRowView {
+    const T *row;
+    const uint4 *body;  // the 16-byte-aligned body
+    uint32_t bytes;     // its length
+    int body0, head0, tail0, nhead, ntail;
+    __device__ RkRowView(const T *r, int V) : row(r) {
+        const SliceSplit sp = split_slice(r, 0, V);
+        body = reinterpret_cast<const uint4 *>(r + sp.body0);
+        bytes = (uint32_t)(sp.tail0 - sp.body0) * (uint32_t)sizeof(T);
+        body0 = sp.body0;
+        head0 = sp.head0;
+        tail0 = sp.tail0;
+        nhead = sp.body0 - sp.head0;
+        ntail = sp.hi - sp.tail0;
+    }
+    __device__ __forceinline__ void prefetch_group(int c) const {
+        const uint32_t off = (uint32_t)c * kRkCH;
+        const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
+#pragma unroll
+        for (int i = 0; i < kRkVec; ++i) {
+            const int qv = (int)threadIdx.x + i * kNT;
+            if (qv < nv) prefetch_l2(body + (int64_t)c * (kRkCH / 16) + qv);
+        }
+    }
+    // group (chunk c, this thread): its vectors, -inf past the body (a chunk
+    // index past the row, from a pass that did not finish, reads nothing)
+    __device__ __forceinline__ void load_group(int c, uint4 (&v)[kRkVec]) const {
+        const uint32_t off = (uint32_t)c * kRkCH;
+        const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
+#pragma unroll
+        for (int i = 0; i < kRkVec; ++i) {
+            const int qv = (int)threadIdx.x + i * kNT;
+            v[i] = qv < nv ? __ldg(body + (int64_t)c * (kRkCH / 16) + qv) : vec_neg_inf<T>();
+        }
+    }
+};
+
+// one slot range per warp (a single shared atomic per warp: the threads'
+// atomics on one word would serialize); every lane calls it
+__device__ __forceinline__ unsigned warp_reserve(unsigned n, int *cnt) {
+    const int lane = threadIdx.x & 31;
+    unsigned incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    unsigned base = 0u;
+    if (lane == 31 && incl) base = (unsigned)atomicAdd(cnt, (int)incl);
+    return __shfl_sync(kFull, base, 31) + incl - n;
+}
+
+// the elements of group c that reach tf (bits of hm), from `at` on
+template <typename T>
+__device__ __forceinline__ void write_group(uint2 *cand, unsigned &at, int body0, int c, const uint4 (&v)[kRkVec],
+                                            uint32_t hm) {
+    constexpr int VEC = Elem<T>::VEC;
+    constexpr int ECH = kRkCH / (int)sizeof(T);
+    const int vbase = body0 + c * ECH;
+#pragma unroll
+    for (int i = 0; i < kRkVec; ++i) {
+        uint32_t h = (hm >> (VEC * i)) & ((1u << VEC) - 1u);
+        while (h) {
+            const int e = __ffs(h) - 1;
+            h &= h - 1u;
+            if (at < (unsigned)kRkCap)
+                cand[at] = make_uint2(kkey<T>(vec_elem<T>(v[i], e)), (uint32_t)(vbase + ((int)threadIdx.x + i * kNT) * VEC + e));
+            ++at;
+        }
+    }
+}
+template <typename T>
+__device__ __forceinline__ uint32_t group_hits(const uint4 (&v)[kRkVec], float tf) {
+    constexpr int VEC = Elem<T>::VEC;
+    uint32_t hm = 0u;
+#pragma unroll
+    for (int i = 0; i < kRkVec; ++i) hm |= vec_ge_mask<T>(v[i], tf) << (VEC * i);
+    return hm;
+}
+
+// The decision: one block per position.
+template <typename T>
+__global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams p) {
+    __shared__ SampBase sb;
+    __shared__ RkRed rd;
+    __shared__ int s_cnt[2];  // candidates listed per row (may pass kRkCap: then some were lost)
+    __shared__ RkInputs s_in;
+    __shared__ RkPairRed pr;
+    __shared__ __align__(16) float4 s_red4[kNW];
+    extern __shared__ __align__(128) unsigned char dsm[];
+    RkDecide &D = *reinterpret_cast<RkDecide *>(dsm);
+    uint2 *cand = reinterpret_cast<uint2 *>(dsm + kRkCandOff);  // [2][kRkCap]
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const unsigned K = (unsigned)p.top_k;
+    const int g = p.gamma;
+    const int pos = blockIdx.x, b = pos / (g + 1), k = pos - b * (g + 1);
+    const int rows = k < g ? 2 : 1;
+    const bool nucleus = p.top_p > 0.0f && p.top_p < 1.0f;
+    load_exp_tables(p, sb);
+    const DdExpTables &EK = sb.K;
+    if (tid < 2) s_cnt[tid] = 0;
+    // what does not depend on the pass: the position's inputs, the rows'
+    // head and tail scalars
+    if (tid == 0) {
+        s_in.d = k < g ? p.tokens[(int64_t)b * g + k] : 0;
+        s_in.u_k = k < g ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
+        s_in.u_f = p.unif[(int64_t)b * (g + 1) + g];
+    }
+    const RkRowView<T> V0(reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride, p.V);
+    const RkRowView<T> V1(k < g ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride
+                                : reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride, p.V);
+    float xh[2], xt[2];
+    xh[0] = tid < V0.nhead ? ld_elem(V0.row, V0.head0 + tid) : -INFINITY;
+    xt[0] = tid < V0.ntail ? ld_elem(V0.row, V0.tail0 + tid) : -INFINITY;
+    xh[1] = rows > 1 && tid < V1.nhead ? ld_elem(V1.row, V1.head0 + tid) : -INFINITY;
+    xt[1] = rows > 1 && tid < V1.ntail ? ld_elem(V1.row, V1.tail0 + tid) : -INFINITY;
+
+    pdl_wait_primary();  // the pass's results (and this call's rejection words) from here on
+    const unsigned rejw = tid == 0 ? *((volatile unsigned *)&p.rejword[b]) : 0u;
+    uint32_t km[2] = {0u, 0u}, t4[2][4];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int64_t slot = (int64_t)pos * 2 + rr;
+        const bool on = rr < rows;
+        km[rr] = on ? __ldcg(p.rkmax + slot * kNT + tid) : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) t4[rr][j] = on ? __ldcg(p.rkgrp + (slot * 4 + j) * kNT + tid) : 0u;
+    }
+    if (tid == 0) s_in.rej = rejw;
+    // theta per row: the K-th largest thread maximum (0 with fewer than K
+    // finite ones: every group is listed, the kept set is every finite logit)
+    constexpr int KB = Elem<T>::KEY_BITS;
+    uint32_t th16[2], theta[2];
+    float tf[2];
+    block_kth_pair<KB>(km[0], km[1], K, pr, theta[0], theta[1]);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        th16[rr] = theta[rr] >> (KB - 16);
+        tf[rr] = fmaxf(key_value<T>(theta[rr]), lowest_finite<T>());
+    }
+    auto is_cand = [&](int rr, uint32_t t) { return t != 0u && (t >> 16) >= th16[rr]; };
+    // a thread whose fourth group qualifies may have more: the exact path
+    const bool over = is_cand(0, t4[0][3]) || (rows > 1 && is_cand(1, t4[1][3]));
+    bool exact = __syncthreads_or(over);  // block-uniform
+    if (!exact) {
+        // ---- the listing: group j of both rows in flight together, j = 0, 1 ----
+        // (the second groups, where they qualify, go into L2 at once)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+            if (rr < rows && is_cand(rr, t4[rr][1])) (rr ? V1 : V0).prefetch_group((int)(t4[rr][1] & 0xffffu));
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            uint4 v[2][kRkVec];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+                if (rr < rows && is_cand(rr, t4[rr][j])) (rr ? V1 : V0).load_group((int)(t4[rr][j] & 0xffffu), v[rr]);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                if (rr >= rows) break;  // block-uniform
+                const RkRowView<T> &W = rr ? V1 : V0;
+                const uint32_t hm = is_cand(rr, t4[rr][j]) ? group_hits<T>(v[rr], tf[rr]) : 0u;
+                // the head and tail scalars with the first group
+                const bool hh = j == 0 && xh[rr] >= tf[rr], ht = j == 0 && xt[rr] >= tf[rr];
+                unsigned at = warp_reserve((unsigned)__popc(hm) + (hh ? 1u : 0u) + (ht ? 1u : 0u), &s_cnt[rr]);
+                uint2 *cb = cand + rr * kRkCap;
+                if (hm) write_group<T>(cb, at, W.body0, (int)(t4[rr][j] & 0xffffu), v[rr], hm);
+                if (hh) {
+                    if (at < (unsigned)kRkCap) cb[at] = make_uint2(kkey<T>(xh[rr]), (uint32_t)(W.head0 + tid));
+                    ++at;
+                }
+                if (ht && at < (unsigned)kRkCap) cb[at] = make_uint2(kkey<T>(xt[rr]), (uint32_t)(W.tail0 + tid));
+            }
+            // the second groups: only when some thread has one
+            if (j == 0 && !__syncthreads_or(is_cand(0, t4[0][1]) || (rows > 1 && is_cand(1, t4[1][1])))) break;
+        }
+        // the third candidate group (rare)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr >= rows) break;
+            const bool c2 = is_cand(rr, t4[rr][2]);
+            if (!__syncthreads_or(c2)) continue;  // block-uniform
+            uint4 v2[kRkVec];
+            const RkRowView<T> &W = rr ? V1 : V0;
+            if (c2) W.load_group((int)(t4[rr][2] & 0xffffu), v2);
+            const uint32_t hm = c2 ? group_hits<T>(v2, tf[rr]) : 0u;
+            unsigned at = warp_reserve((unsigned)__popc(hm), &s_cnt[rr]);
+            if (hm) write_group<T>(cand + rr * kRkCap, at, W.body0, (int)(t4[rr][2] & 0xffffu), v2, hm);
+        }
+        __syncthreads();  // every listed entry is in the buffers
+
+        // ---- the kept sets: exact threshold, token order, statistics ----
+        // Half a block per row: thread t holds entries u, u + 128, ... of row
+        // t / 128 (u = t % 128).  An entry is kept iff fewer than K listed
+        // entries of its row are larger: exactly the entries >= the K-th
+        // largest (ties included).  Only warps holding entries scan the list.
+        constexpr int HALF = kNT / 2, HW = HALF / 32, PER = kRkCap / HALF;
+        const int rr = tid / HALF, u = tid % HALF;
+        int cnt[2];
+        bool ovf[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            cnt[x] = x < rows ? s_cnt[x] : 0;
+            ovf[x] = cnt[x] > kRkCap;
+        }
+        const int n = ovf[rr] ? 0 : cnt[rr];
+        const uint2 *cb = cand + rr * kRkCap;
+        uint2 e[PER];
+        bool f[PER];
+        unsigned nk = 0u;
+        uint32_t mx = 0u, lo = 0xffffffffu;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            e[i] = u + i * HALF < n ? cb[u + i * HALF] : make_uint2(0u, 0u);
+            f[i] = false;
+        }
+        if (__any_sync(kFull, u < n)) {
+            unsigned gr[PER] = {};
+            if (n <= HALF) {  // one entry per thread (the usual case)
+                for (int y = 0; y < n; ++y) gr[0] += cb[y].x > e[0].x ? 1u : 0u;
+            } else {
+                for (int y = 0; y < n; ++y) {
+                    const uint32_t ky = cb[y].x;
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) gr[i] += ky > e[i].x ? 1u : 0u;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                f[i] = e[i].x != 0u && gr[i] < K;
+                nk += f[i] ? 1u : 0u;
+                mx = max(mx, e[i].x);
+                if (f[i]) lo = min(lo, e[i].x);
+            }
+        }
+        // per half: kept count, largest key, smallest kept key
+        nk = __reduce_add_sync(kFull, nk);
+        mx = __reduce_max_sync(kFull, mx);
+        lo = __reduce_min_sync(kFull, lo);
+        if (lane == 0) {
+            rd.u[0][wid] = nk;
+            rd.u[1][wid] = mx;
+            pr.c[0][wid][0] = lo;
+        }
+        unsigned char *kflag = reinterpret_cast<unsigned char *>(D.prb);  // [2][kRkCap] kept flags (free until top-p)
+        static_assert(sizeof(D.prb) >= 2 * kRkCap, "kept flags fit");
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (u + i * HALF < n) kflag[rr * kRkCap + u + i * HALF] = f[i];
+        __syncthreads();
+        unsigned kn_r = 0u;
+        uint32_t mk_r = 0u, th_r = 0xffffffffu;
+#pragma unroll
+        for (int w = 0; w < HW; ++w) {
+            kn_r += rd.u[0][rr * HW + w];
+            mk_r = max(mk_r, rd.u[1][rr * HW + w]);
+            th_r = min(th_r, pr.c[0][rr * HW + w][0]);
+        }
+        th_r = (unsigned)n >= K ? th_r : 0u;
+        const bool big = kn_r > (unsigned)kKeptMax;
+        // token order among the kept entries of the row; the normaliser's terms
+        const float m = kn_r > 0u ? key_value<T>(mk_r) : -INFINITY;
+        dd t{0.0f, 0.0f};
+        bool anyf = false;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) anyf = anyf || f[i];
+        if (!big && __any_sync(kFull, anyf)) {
+            unsigned rk[PER] = {};
+            const unsigned char *kf = kflag + rr * kRkCap;
+            if (n <= HALF) {
+                for (int y = 0; y < n; ++y) rk[0] += (kf[y] && cb[y].y < e[0].y) ? 1u : 0u;
+            } else {
+                for (int y = 0; y < n; ++y) {
+                    if (!kf[y]) continue;
+                    const uint32_t ty = cb[y].y;
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) rk[i] += ty < e[i].y ? 1u : 0u;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                if (f[i]) {
+                    D.kept[rr][rk[i]] = e[i];
+                    t = dd_add(t, dd_expw(key_value<T>(e[i].x), m, EK));
+                }
+        }
+        dd Sp[2] = {rr == 0 ? t : dd{0.0f, 0.0f}, rr == 1 ? t : dd{0.0f, 0.0f}};
+        if (u == 0) {  // one thread per half: the row's statistics
+            D.m[rr] = m;
+            D.kn[rr] = kn_r;
+            D.th[rr] = th_r;
+        }
+        // the kept count of both rows, for the exact-path decision
+        const bool big0 = __syncthreads_or(rr == 0 && big), big1 = __syncthreads_or(rr == 1 && big);
+        ovf[0] = ovf[0] || big0;
+        ovf[1] = ovf[1] || big1;
+        int kn[2];
+        uint32_t th[2];
+        kn[0] = (int)D.kn[0];
+        kn[1] = (int)D.kn[1];
+        th[0] = D.th[0];
+        th[1] = D.th[1];
+        // both rows' normalisers in one block reduction
+        block_dd_sum2<kNT>(Sp[0], Sp[1], s_red4);
+        if (ovf[0] || (rows > 1 && ovf[1])) exact = true;  // block-uniform
+        if (!exact) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                if (x >= rows) break;
+                int knr = kn[x];
+                uint32_t thr = th[x];
+                dd S = Sp[x];
+                if (nucleus && D.m[x] != -INFINITY) {
+                    __syncthreads();  // the kept set is in place
+                    if (wid == 0) {
+                        row_top_p<T>(D.kept[x], knr, thr, D.m[x], S, p.top_p, D.tmp, D.prb, EK);
+                        if (lane == 0) {
+                            D.kn[x] = (unsigned)knr;
+                            D.th[x] = thr;
+                            D.S[x] = make_float2(S.hi, S.lo);
+                        }
+                    }
+                } else if (tid == 0) {
+                    D.kn[x] = (unsigned)knr;
+                    D.th[x] = thr;
+                    D.S[x] = make_float2(S.hi, S.lo);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (exact) {  // the decision arrays and buffers are free: the exact path's ring
+        rk_exact_position<T>(p, sb, dsm, k, b);
+    } else {
+        const Outcome o = block_outcome<T>(p, b, k, D, EK, rd, s_red4, s_in);
+        finish(p, b, k, o, sb);
+    }
+}
+
+template <typename T>
+static cudaError_t launch_topk(const SampleParams &p, int sms, cudaStream_t s) {
+    static std::atomic<unsigned long long> done_pass{0}, done_decide{0};
+    constexpr size_t pass_dyn = sizeof(RkRing);
+    cudaError_t e = ensure_smem_attr(chain_topk_pass_kernel<T>, (int)pass_dyn, done_pass);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attr(chain_topk_decide_kernel<T>, (int)kRkDecideDyn, done_decide);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_topk_row_kernel<T>, kNT, kRkDyn);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_topk_pass_kernel<T>, kNT, pass_dyn);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t rows = (int64_t)p.B * (2 * p.gamma + 1);
     const int64_t cap = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(rows < cap ? rows : cap);
-    chain_topk_row_kernel<T><<<grid, kNT, kRkDyn, s>>>(p);
-    return cudaGetLastError();
+    chain_topk_pass_kernel<T><<<grid, kNT, pass_dyn, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)p.B * (p.gamma + 1)));
+    cfg.blockDim = dim3(kNT);
+    cfg.dynamicSmemBytes = kRkDecideDyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chain_topk_decide_kernel<T>, p);
 }
 
 cudaError_t launch_chain_topk(const SampleParams &p, int dtype, int sms, cudaStream_t s) {
-    return dtype == SPEC_DTYPE_BF16 ? launch_rows<__nv_bfloat16>(p, sms, s) : launch_rows<float>(p, sms, s);
+    return dtype == SPEC_DTYPE_BF16 ? launch_topk<__nv_bfloat16>(p, sms, s) : launch_topk<float>(p, sms, s);
 }
 
 }  // namespace specv

@@ -86,10 +86,10 @@ def test_workspace_sizes(lib):
     assert L.spec_workspace_bytes(L.SPEC_WS_TREE, 128, 5, 128256) >= 256 + 128 * 4 + 128 * 5 * 8
     assert L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 512, 0, 0) >= 256 + 512 * 4
     base = L.spec_workspace_bytes(L.SPEC_WS_CHAIN, 64, 4, 128256)
-    # the top-k path: per position an arrival counter, and per row a 32-byte
-    # header and 256 kept entries of 8 bytes
+    # the top-k path: per position two row slots, each with 256 thread maxima
+    # and 4 x 256 packed groups of 4 bytes
     assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 64, 4, 128256) >= \
-        base + 64 * 5 * (4 + 2 * (32 + 256 * 8))
+        base + 64 * 5 * 2 * (256 * 4 + 4 * 256 * 4)
     assert L.spec_workspace_bytes(99, 1, 1, 1) == 0
     assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN, -1, 1, 1) == 0
 
