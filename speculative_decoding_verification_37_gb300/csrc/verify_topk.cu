@@ -48,6 +48,7 @@ constexpr int kRkCH = 16384;              // bytes of a row's body per ring stag
 constexpr int kRkNST = 3;                 // ring stages
 constexpr int kRkCap = 512;               // candidate entries a row can hold
 constexpr int kRkBlocksPerSM = 4;         // pass blocks per SM
+constexpr int kRkGroupCap = 1024;         // candidate groups a position can list
 constexpr int kRkVec = kRkCH / 16 / kNT;  // 16-byte vectors per thread and chunk
 static_assert(kRkVec * 16 * kNT == kRkCH, "a chunk is whole vectors per thread");
 static_assert(kRkVec * 8 <= 32, "a thread's hit bits fit one word");
@@ -68,6 +69,8 @@ struct RkDecide {
     unsigned kn[2], th[2], flags[2];
     float m[2];
     float2 S[2];
+    float a;        // a_k, written by the thread holding d's kept target entry
+    unsigned ahit;  // 1 once it has
 };
 constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
 // a decide block's dynamic shared memory: the decision arrays and both rows'
@@ -422,33 +425,10 @@ __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int 
     if (bad_tok || bad_row) return o;
     const dd isp = dd_recip(sp);
     const dd isq = has_draft ? dd_recip(sq) : dd{0.0f, 0.0f};
-    bool accept = false;
-    if (has_draft) {
-        // p(d), q(d): d's entry in each kept set (token order), 0 when d is not kept
-        auto find = [&](const uint2 *kp, int n) -> int {
-            int lo = 0, hi = n;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (kp[mid].y < (uint32_t)d) lo = mid + 1; else hi = mid;
-            }
-            return lo < n && kp[lo].y == (uint32_t)d ? lo : -1;
-        };
-        const int ip = find(Kp, np), iq = find(Kq, nq);
-        const dd pd = ip >= 0 ? dd_mul(dd_expw(key_value<T>(Kp[ip].x), mp, EK), isp) : dd{0.0f, 0.0f};
-        const dd qd = iq >= 0 ? dd_mul(dd_expw(key_value<T>(Kq[iq].x), mq, EK), isq) : dd{0.0f, 0.0f};
-        float a;
-        if (dd_pos(qd)) {
-            const dd ratio = dd_mul(pd, dd_recip(qd));
-            a = dd_gt(ratio, dd{1.0f, 0.0f}) ? 1.0f : dd_to_f(ratio);
-        } else {
-            a = dd_pos(pd) ? 1.0f : 0.0f;
-        }
-        o.a = a;
-        accept = u_k < a;
-        o.info |= accept ? REC_ACCEPT : 0u;
-    }
     // thread t: kept target entry t (token order), its p (the unnormalised
-    // term for the bonus draw) and residual weight max(0, p - q)
+    // term for the bonus draw) and residual weight max(0, p - q).  The thread
+    // holding d's entry also forms a_k = min(1, p(d)/q(d)); d outside the
+    // target's kept set has p(d) = 0, so a_k = 0 (D.ahit stays 0).
     dd pi{0.0f, 0.0f}, w{0.0f, 0.0f};
     if (tid < np) {
         const dd ex = dd_expw(key_value<T>(Kp[tid].x), mp, EK);
@@ -464,15 +444,31 @@ __device__ __noinline__ Outcome block_outcome(const SampleParams &p, int b, int 
             }
             const dd qi = (lo < nq && Kq[lo].y == id) ? dd_mul(dd_expw(key_value<T>(Kq[lo].x), mq, EK), isq)
                                                      : dd{0.0f, 0.0f};
+            if (id == (uint32_t)d) {
+                float a;
+                if (dd_pos(qi)) {
+                    const dd ratio = dd_mul(pi, dd_recip(qi));
+                    a = dd_gt(ratio, dd{1.0f, 0.0f}) ? 1.0f : dd_to_f(ratio);
+                } else {
+                    a = dd_pos(pi) ? 1.0f : 0.0f;
+                }
+                D.a = a;
+                D.ahit = 1u;
+            }
             w = dd_max0(dd_add(pi, dd_neg(qi)));
         }
     }
     dd zw{0.0f, 0.0f}, zp{0.0f, 0.0f};
-    if (has_draft) {  // both sums in one block reduction
+    bool accept = false;
+    if (has_draft) {  // both sums in one block reduction (its barriers publish D.a)
         zw = w;
         zp = pi;
         block_dd_sum2<kNT>(zw, zp, red4);
         o.z = dd_to_f(zw);
+        const float a = D.ahit ? D.a : 0.0f;
+        o.a = a;
+        accept = u_k < a;
+        o.info |= accept ? REC_ACCEPT : 0u;
     }
     const bool earlier = rej > (unsigned)(g - k + 1);
     if (has_draft && !accept && tid == 0) atomicMax(p.rejword + b, (unsigned)(g - k + 1));
@@ -652,6 +648,16 @@ struct RkRowView {
             if (qv < nv) prefetch_l2(body + (int64_t)c * (kRkCH / 16) + qv);
         }
     }
+    // group (chunk c, thread t): its vectors, -inf past the body
+    __device__ __forceinline__ void load_group_of(int c, int t, uint4 (&v)[kRkVec]) const {
+        const uint32_t off = (uint32_t)c * kRkCH;
+        const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
+#pragma unroll
+        for (int i = 0; i < kRkVec; ++i) {
+            const int qv = t + i * kNT;
+            v[i] = qv < nv ? __ldg(body + (int64_t)c * (kRkCH / 16) + qv) : vec_neg_inf<T>();
+        }
+    }
     // group (chunk c, this thread): its vectors, -inf past the body (a chunk
     // index past the row, from a pass that did not finish, reads nothing)
     __device__ __forceinline__ void load_group(int c, uint4 (&v)[kRkVec]) const {
@@ -699,6 +705,25 @@ __device__ __forceinline__ void write_group(uint2 *cand, unsigned &at, int body0
         }
     }
 }
+// the same for group (c, t) of another thread
+template <typename T>
+__device__ __forceinline__ void write_group_of(uint2 *cand, unsigned &at, int body0, int c, int t, const uint4 (&v)[kRkVec],
+                                               uint32_t hm) {
+    constexpr int VEC = Elem<T>::VEC;
+    constexpr int ECH = kRkCH / (int)sizeof(T);
+    const int vbase = body0 + c * ECH;
+#pragma unroll
+    for (int i = 0; i < kRkVec; ++i) {
+        uint32_t h = (hm >> (VEC * i)) & ((1u << VEC) - 1u);
+        while (h) {
+            const int e = __ffs(h) - 1;
+            h &= h - 1u;
+            if (at < (unsigned)kRkCap)
+                cand[at] = make_uint2(kkey<T>(vec_elem<T>(v[i], e)), (uint32_t)(vbase + (t + i * kNT) * VEC + e));
+            ++at;
+        }
+    }
+}
 template <typename T>
 __device__ __forceinline__ uint32_t group_hits(const uint4 (&v)[kRkVec], float tf) {
     constexpr int VEC = Elem<T>::VEC;
@@ -714,6 +739,8 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
     __shared__ SampBase sb;
     __shared__ RkRed rd;
     __shared__ int s_cnt[2];  // candidates listed per row (may pass kRkCap: then some were lost)
+    __shared__ int s_ng;      // candidate groups of the position
+    __shared__ uint32_t glist[kRkGroupCap];  // (row << 31 | chunk << 8 | owner thread)
     __shared__ RkInputs s_in;
     __shared__ RkPairRed pr;
     __shared__ __align__(16) float4 s_red4[kNW];
@@ -729,6 +756,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
     load_exp_tables(p, sb);
     const DdExpTables &EK = sb.K;
     if (tid < 2) s_cnt[tid] = 0;
+    if (tid == 0) s_ng = 0;
     // what does not depend on the pass: the position's inputs, the rows'
     // head and tail scalars
     if (tid == 0) {
@@ -773,48 +801,63 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
     const bool over = is_cand(0, t4[0][3]) || (rows > 1 && is_cand(1, t4[1][3]));
     bool exact = __syncthreads_or(over);  // block-uniform
     if (!exact) {
-        // ---- the listing: group j of both rows in flight together, j = 0, 1 ----
-        // (the second groups, where they qualify, go into L2 at once)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-            if (rr < rows && is_cand(rr, t4[rr][1])) (rr ? V1 : V0).prefetch_group((int)(t4[rr][1] & 0xffffu));
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            uint4 v[2][kRkVec];
+        // ---- the listing ----
+        // 1. the candidate groups of both rows, (row, chunk, owner thread),
+        //    into one shared list; 2. one group per thread: its vectors
+        //    reloaded (all in flight at once) and its elements >= tf listed.
+        //    The head and tail scalars are listed by their own threads.
+        {
+            unsigned ng = 0u;
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr)
-                if (rr < rows && is_cand(rr, t4[rr][j])) (rr ? V1 : V0).load_group((int)(t4[rr][j] & 0xffffu), v[rr]);
+#pragma unroll
+                for (int j = 0; j < 3; ++j) ng += (rr < rows && is_cand(rr, t4[rr][j])) ? 1u : 0u;
+            unsigned at = warp_reserve(ng, &s_ng);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    if (rr < rows && is_cand(rr, t4[rr][j])) {
+                        if (at < (unsigned)kRkGroupCap)
+                            glist[at] = ((uint32_t)rr << 31) | ((t4[rr][j] & 0xffffu) << 8) | (uint32_t)tid;
+                        ++at;
+                    }
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 if (rr >= rows) break;  // block-uniform
                 const RkRowView<T> &W = rr ? V1 : V0;
-                const uint32_t hm = is_cand(rr, t4[rr][j]) ? group_hits<T>(v[rr], tf[rr]) : 0u;
-                // the head and tail scalars with the first group
-                const bool hh = j == 0 && xh[rr] >= tf[rr], ht = j == 0 && xt[rr] >= tf[rr];
-                unsigned at = warp_reserve((unsigned)__popc(hm) + (hh ? 1u : 0u) + (ht ? 1u : 0u), &s_cnt[rr]);
+                const bool hh = xh[rr] >= tf[rr], ht = xt[rr] >= tf[rr];
+                unsigned ah = warp_reserve((hh ? 1u : 0u) + (ht ? 1u : 0u), &s_cnt[rr]);
                 uint2 *cb = cand + rr * kRkCap;
-                if (hm) write_group<T>(cb, at, W.body0, (int)(t4[rr][j] & 0xffffu), v[rr], hm);
                 if (hh) {
-                    if (at < (unsigned)kRkCap) cb[at] = make_uint2(kkey<T>(xh[rr]), (uint32_t)(W.head0 + tid));
-                    ++at;
+                    if (ah < (unsigned)kRkCap) cb[ah] = make_uint2(kkey<T>(xh[rr]), (uint32_t)(W.head0 + tid));
+                    ++ah;
                 }
-                if (ht && at < (unsigned)kRkCap) cb[at] = make_uint2(kkey<T>(xt[rr]), (uint32_t)(W.tail0 + tid));
+                if (ht && ah < (unsigned)kRkCap) cb[ah] = make_uint2(kkey<T>(xt[rr]), (uint32_t)(W.tail0 + tid));
             }
-            // the second groups: only when some thread has one
-            if (j == 0 && !__syncthreads_or(is_cand(0, t4[0][1]) || (rows > 1 && is_cand(1, t4[1][1])))) break;
         }
-        // the third candidate group (rare)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            if (rr >= rows) break;
-            const bool c2 = is_cand(rr, t4[rr][2]);
-            if (!__syncthreads_or(c2)) continue;  // block-uniform
-            uint4 v2[kRkVec];
-            const RkRowView<T> &W = rr ? V1 : V0;
-            if (c2) W.load_group((int)(t4[rr][2] & 0xffffu), v2);
-            const uint32_t hm = c2 ? group_hits<T>(v2, tf[rr]) : 0u;
-            unsigned at = warp_reserve((unsigned)__popc(hm), &s_cnt[rr]);
-            if (hm) write_group<T>(cand + rr * kRkCap, at, W.body0, (int)(t4[rr][2] & 0xffffu), v2, hm);
+        __syncthreads();
+        {
+            const int ngr = min(s_ng, kRkGroupCap);
+            for (int g0 = 0; g0 < ngr; g0 += kNT) {  // (block-uniform trip count)
+                const int gi = g0 + tid;
+                const bool on = gi < ngr;
+                const uint32_t ge = on ? glist[gi] : 0u;
+                const int rr = (int)(ge >> 31), c = (int)((ge >> 8) & 0xffffu), owner = (int)(ge & 0xffu);
+                uint4 v[kRkVec];
+                if (on) (rr ? V1 : V0).load_group_of(c, owner, v);
+                const float tfr = rr ? tf[1] : tf[0];
+                const uint32_t hm = on ? group_hits<T>(v, tfr) : 0u;
+                // slots per row: a warp reserves for each row its lanes' hits
+                const unsigned a0 = warp_reserve(rr == 0 ? (unsigned)__popc(hm) : 0u, &s_cnt[0]);
+                const unsigned a1 = warp_reserve(rr == 1 ? (unsigned)__popc(hm) : 0u, &s_cnt[1]);
+                if (hm) {
+                    unsigned a = rr ? a1 : a0;
+                    write_group_of<T>(cand + rr * kRkCap, a, (rr ? V1 : V0).body0, c, owner, v, hm);
+                }
+            }
+            // more candidate groups than the list holds: the exact path
+            if (s_ng > (unsigned)kRkGroupCap) s_cnt[0] = kRkCap + 1;
         }
         __syncthreads();  // every listed entry is in the buffers
 
@@ -918,29 +961,23 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
             D.m[rr] = m;
             D.kn[rr] = kn_r;
             D.th[rr] = th_r;
+            if (rr == 0) D.ahit = 0u;
         }
-        // the kept count of both rows, for the exact-path decision
-        const bool big0 = __syncthreads_or(rr == 0 && big), big1 = __syncthreads_or(rr == 1 && big);
-        ovf[0] = ovf[0] || big0;
-        ovf[1] = ovf[1] || big1;
-        int kn[2];
-        uint32_t th[2];
-        kn[0] = (int)D.kn[0];
-        kn[1] = (int)D.kn[1];
-        th[0] = D.th[0];
-        th[1] = D.th[1];
-        // both rows' normalisers in one block reduction
+        // both rows' normalisers in one block reduction (its barriers also
+        // publish D.kn, D.th, D.m); a kept set too large for the arrays, in
+        // either row, sends the position to the exact path
+        const bool anybig = __syncthreads_or(big);
         block_dd_sum2<kNT>(Sp[0], Sp[1], s_red4);
-        if (ovf[0] || (rows > 1 && ovf[1])) exact = true;  // block-uniform
+        if (anybig || ovf[0] || (rows > 1 && ovf[1])) exact = true;  // block-uniform
         if (!exact) {
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 if (x >= rows) break;
-                int knr = kn[x];
-                uint32_t thr = th[x];
                 dd S = Sp[x];
                 if (nucleus && D.m[x] != -INFINITY) {
-                    __syncthreads();  // the kept set is in place
+                    int knr = (int)D.kn[x];
+                    uint32_t thr = D.th[x];
+                    __syncthreads();  // the kept set is in place; every thread has read D.kn/th
                     if (wid == 0) {
                         row_top_p<T>(D.kept[x], knr, thr, D.m[x], S, p.top_p, D.tmp, D.prb, EK);
                         if (lane == 0) {
@@ -950,8 +987,6 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
                         }
                     }
                 } else if (tid == 0) {
-                    D.kn[x] = (unsigned)knr;
-                    D.th[x] = thr;
                     D.S[x] = make_float2(S.hi, S.lo);
                 }
             }
