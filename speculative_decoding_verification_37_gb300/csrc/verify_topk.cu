@@ -889,6 +889,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
         if (__any_sync(kFull, u < n)) {
             unsigned gr[PER] = {};
             if (n <= HALF) {  // one entry per thread (the usual case)
+#pragma unroll 8
                 for (int y = 0; y < n; ++y) gr[0] += cb[y].x > e[0].x ? 1u : 0u;
             } else {
                 for (int y = 0; y < n; ++y) {
@@ -940,6 +941,7 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
             unsigned rk[PER] = {};
             const unsigned char *kf = kflag + rr * kRkCap;
             if (n <= HALF) {
+#pragma unroll 8
                 for (int y = 0; y < n; ++y) rk[0] += (kf[y] && cb[y].y < e[0].y) ? 1u : 0u;
             } else {
                 for (int y = 0; y < n; ++y) {
