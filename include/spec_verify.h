@@ -86,7 +86,8 @@ extern "C" {
 #define SPEC_WS_TREE 1  /* n = R (logits rows per request) */
 #define SPEC_WS_COMMIT 2
 #define SPEC_WS_CHAIN_TOPK 3 /* n = gamma: SPEC_WS_CHAIN plus what the fast top-k path's pass
-                                hands its decision (10 KiB per request position) (0 < top_k <= 128) */
+                                hands its decision and the published kept sets (about 14 KiB per
+                                request position) (0 < top_k <= 128) */
 #define SPEC_WS_CHAIN_FULL 4 /* n = gamma: SPEC_WS_CHAIN plus the per-slice statistics, draw
                                 state and work queue of the persistent full-vocabulary path
                                 (top_k == 0; about 2 KiB per request position at V = 128,256) */
@@ -124,7 +125,7 @@ extern "C" {
  *   row pair); flags[b].
  * Workspace: spec_workspace_bytes(SPEC_WS_CHAIN, B, gamma, V) bytes suffice
  *   for every call.  Sampled calls with 0 < top_k <= 128 take a faster path
- *   (a maxima-only pass over the rows, then one block per position) when
+ *   (a maxima-only pass over the rows, then one decision block per row) when
  *   the workspace holds
  *   spec_workspace_bytes(SPEC_WS_CHAIN_TOPK, B, gamma, V) bytes; with less
  *   they take the exact cluster-wide threshold search instead.  Sampled calls

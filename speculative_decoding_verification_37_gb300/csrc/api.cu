@@ -76,6 +76,9 @@ struct Ws {
     void *data;          // chain: records or argmax keys; tree: argmax keys
     uint32_t *rkmax;     // chain, top-k: [B*(gamma+1)*2][kTopKThreads] thread maxima
     uint32_t *rkgrp;     // chain, top-k: [B*(gamma+1)*2][kTopKGroups][kTopKThreads] largest groups
+    TopkRow *rkrow;      // chain, top-k: [B*(gamma+1)*2] published kept-set headers
+    uint2 *rkent;        // chain, top-k: [B*(gamma+1)*2][kKeptRowMax] kept entries
+    unsigned *rkcnt;     // chain, top-k: [B*(gamma+1)] position arrival counters (zeroed)
     // chain, full vocabulary: see SampleParams
     float2 *fpart, *fxd;
     float4 *fstat;
@@ -120,9 +123,15 @@ size_t ws_layout_bytes(int B, size_t rows, size_t data_bytes, Ws *w, void *base_
     if (extra == kWsPool) {
         char *rm = take(rows * 2 * (size_t)kTopKThreads * sizeof(uint32_t));
         char *rg = take(rows * 2 * (size_t)kTopKGroups * kTopKThreads * sizeof(uint32_t));
+        char *rh = take(rows * 2 * sizeof(TopkRow));
+        char *re = take(rows * 2 * (size_t)kKeptRowMax * sizeof(uint2));
+        char *rc = take(rows * sizeof(unsigned));
         if (w) {
             w->rkmax = reinterpret_cast<uint32_t *>(rm);
             w->rkgrp = reinterpret_cast<uint32_t *>(rg);
+            w->rkrow = reinterpret_cast<TopkRow *>(rh);
+            w->rkent = reinterpret_cast<uint2 *>(re);
+            w->rkcnt = reinterpret_cast<unsigned *>(rc);
         }
     } else if (extra == kWsFull) {
         const size_t c = (size_t)full_slices(V, SPEC_DTYPE_F32), nb = (size_t)B;
@@ -351,6 +360,9 @@ extern "C" int spec_verify_chain(const SpecChainArgs *a, void *workspace, size_t
         p.recs = static_cast<PosRec *>(w.data);
         p.rkmax = w.rkmax;
         p.rkgrp = w.rkgrp;
+        p.rkrow = w.rkrow;
+        p.rkent = w.rkent;
+        p.rkcnt = w.rkcnt;
         p.fpart = w.fpart;
         p.fxd = w.fxd;
         p.fstat = w.fstat;

@@ -70,6 +70,17 @@ constexpr int kKeptRowMax = 256;   // kept entries of one row a position can hol
 constexpr int kTopKGroups = 4;     // groups per thread the top-k pass hands on
 constexpr int kTopKThreads = 256;  // threads of a top-k pass block
 
+// One row's kept set on the top-k path, published for its position's
+// deciding block (16-byte words, read with two vector loads).
+struct alignas(16) TopkRow {
+    unsigned kn;      // kept entries, token order, in the row's entry array
+    unsigned th;      // order key of the threshold: every kept logit's key is >= it
+    float m;          // largest kept logit (-inf: no finite logit)
+    float s_hi, s_lo; // sum over the kept set of exp((l - m)/T), double-float
+    unsigned flags;   // 1: the kept set did not fit (the position takes the exact path)
+    unsigned pad[2];
+};
+
 // Full-vocabulary persistent path (verify_full.cu): a request's draw record
 // and one (request, slice) result of a draw round.
 struct DrawRec {
@@ -107,6 +118,10 @@ struct SampleParams {
     // groups (key prefix << 16 | chunk), thread-minor
     uint32_t *rkmax;     // [B*(gamma+1)*2][kTopKThreads]
     uint32_t *rkgrp;     // [B*(gamma+1)*2][kTopKGroups][kTopKThreads]
+    // and what a row's decision block hands the position's other block
+    TopkRow *rkrow;      // [B*(gamma+1)*2]
+    uint2 *rkent;        // [B*(gamma+1)*2][kKeptRowMax] (order key, token id), token order
+    unsigned *rkcnt;     // [B*(gamma+1)] arrivals, zero between calls
     // full-vocabulary persistent path, c = slices of full_row_bytes()
     float2 *fpart;               // [B*(gamma+1)][2][c] (max, sum) per slice
     float2 *fxd;                 // [B*(gamma+1)] target and draft logit at the draft token

@@ -79,11 +79,6 @@ __device__ __forceinline__ bool mbar_drain(unsigned long long *bar, unsigned pha
     return false;
 }
 
-// a hint: bring the line holding `p` into L2 (no register, no wait)
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
 __device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes,
                                          unsigned long long *bar) {

@@ -18,28 +18,32 @@
 // and writes them to the workspace at the row's end: the pass streams at the
 // memory's pace, with nothing else to wait for.
 //
-// chain_topk_decide_kernel: one block per position, launched as a
-// programmatic dependent of the pass (its launch overlaps the pass's tail;
-// it waits for the pass's results before reading them).  Per row:
+// chain_topk_decide_kernel: one block per row, launched as a programmatic
+// dependent of the pass (its launch overlaps the pass's tail; it waits for
+// the pass's results before reading them).  For its row:
 //  1. theta = the k-th largest of the threads' maxima (each is a logit, so at
 //     least k logits reach it: a lower bound of the row's k-th largest).
 //     Only groups whose maximum reaches theta's prefix can hold a kept
 //     logit, and each thread's such groups are among its four largest unless
 //     the fourth qualifies too (ties: then the position takes the exact
-//     path).  Each thread reloads its candidate groups (both rows' loads in
-//     flight together) and lists their elements >= theta, and the head and
-//     tail scalars >= theta, (order key, token id) in a shared buffer;
+//     path).  The candidate groups go into a shared list and each thread
+//     reloads one (all reloads in flight at once) and lists its elements
+//     >= theta, and the head and tail scalars >= theta, (order key, token id)
+//     in a shared buffer;
 //  2. the kept set: an entry is kept iff fewer than k listed entries are
 //     larger, i.e. exactly the logits >= the k-th largest; then token order,
 //     the maximum and the double-float normaliser (and the nucleus when
-//     top_p is set);
-// then a_k = min(1, p(d)/q(d)), the residual mass over the target's kept set
-// (q looked up in the draft's), and the draw where this position decides the
-// token, by a double-float scan in token order; finish() records it and the
-// last position of a request writes the request's outputs.  A position whose
-// candidates do not fit (many logits tied at the threshold) takes the exact
-// masked computation over both rows instead, the nucleus included (slow,
-// exact, rare).
+//     top_p is set), published to the workspace;
+//  3. the block that arrives second for a position (one counter per
+//     position; the bonus position has one row) reads the other row's kept
+//     set and decides: a_k = min(1, p(d)/q(d)), the residual mass over the
+//     target's kept set (q looked up in the draft's), and the draw where
+//     this position decides the token, by a double-float scan in token
+//     order; finish() records it and the last position of a request writes
+//     the request's outputs.
+// A position whose candidates do not fit (many logits tied at the
+// threshold) takes the exact masked computation over both rows instead, the
+// nucleus included (slow, exact, rare).
 #include "sample_common.cuh"
 
 namespace specv {
@@ -48,7 +52,6 @@ constexpr int kRkCH = 16384;              // bytes of a row's body per ring stag
 constexpr int kRkNST = 3;                 // ring stages
 constexpr int kRkCap = 512;               // candidate entries a row can hold
 constexpr int kRkBlocksPerSM = 4;         // pass blocks per SM
-constexpr int kRkGroupCap = 1024;         // candidate groups a position can list
 constexpr int kRkVec = kRkCH / 16 / kNT;  // 16-byte vectors per thread and chunk
 static_assert(kRkVec * 16 * kNT == kRkCH, "a chunk is whole vectors per thread");
 static_assert(kRkVec * 8 <= 32, "a thread's hit bits fit one word");
@@ -77,7 +80,7 @@ constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
 // candidate buffers, or the exact path's ring
 constexpr size_t kRkCandOff = (sizeof(RkDecide) + 15) / 16 * 16;
 constexpr size_t kRkDecideDyn =
-    (cmax(sizeof(RkFallbackRing), kRkCandOff + 2 * kRkCap * sizeof(uint2)) + 127) / 128 * 128;
+    (cmax(sizeof(RkFallbackRing), kRkCandOff + kRkCap * sizeof(uint2)) + 127) / 128 * 128;
 
 int topk_row_bytes() { return kRkCH; }
 
@@ -178,129 +181,45 @@ struct RkRed {
     float2 f[2][kNW];
 };
 
-// block max / min of one value per thread (every thread gets it)
-__device__ __forceinline__ uint32_t block_max_u(uint32_t v, unsigned *red) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    v = __reduce_max_sync(kFull, v);
-    if (lane == 0) red[wid] = v;
-    __syncthreads();
-    uint32_t t = 0u;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) t = max(t, red[w]);
-    __syncthreads();
-    return t;
-}
-__device__ __forceinline__ uint32_t block_min_u(uint32_t v, unsigned *red) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    v = __reduce_min_sync(kFull, v);
-    if (lane == 0) red[wid] = v;
-    __syncthreads();
-    uint32_t t = 0xffffffffu;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) t = min(t, red[w]);
-    __syncthreads();
-    return t;
-}
-
-// The K-th largest of the keys every thread passes (k0, and k1 when TWO;
-// key 0 means "no key"): the largest r such that at least K keys are >= r,
-// 0 if there are fewer than K keys.  Bits are fixed from the top, below the
-// common prefix of the smallest and largest key, with one block count
-// (__syncthreads_count) per bit.  Every thread calls it and gets the result.
-template <bool TWO>
-__device__ uint32_t block_kth(uint32_t k0, uint32_t k1, unsigned K, RkRed &rd) {
-    const unsigned have = (unsigned)__syncthreads_count(k0 != 0u) + (TWO ? (unsigned)__syncthreads_count(k1 != 0u) : 0u);
-    if (have < K) return 0u;
-    const uint32_t hi = block_max_u(TWO ? max(k0, k1) : k0, rd.u[0]);
-    const uint32_t lo = block_min_u(TWO ? min(k0 ? k0 : 0xffffffffu, k1 ? k1 : 0xffffffffu)
-                                        : (k0 ? k0 : 0xffffffffu), rd.u[1]);
-    if (lo >= hi) return hi;
-    const int nb = 32 - __clz(lo ^ hi);
-    uint32_t res = nb == 32 ? 0u : (hi >> nb) << nb;  // <= lo: every key reaches it
-    for (int bit = nb - 1; bit >= 0; --bit) {
-        const uint32_t c = res | (1u << bit);
-        unsigned n = (unsigned)__syncthreads_count(k0 >= c);
-        if (TWO) n += (unsigned)__syncthreads_count(k1 >= c);
-        if (n >= K) res = c;
-    }
-    return res;
-}
-
-// The K-th largest of two key sets at once (k0: row 0's key of this thread,
-// k1: row 1's; 0 = no key): per set the largest r such that at least K keys
-// are >= r, 0 if the set has fewer than K keys.  Two bits per step, counted
-// with warp ballots and one block barrier (counts double-buffered by step
-// parity).  Every thread calls it and gets both results.
+// Counts exchanged by the block-wide selections below (double-buffered by
+// step parity).
 struct RkPairRed {
     unsigned c[2][kNW][8];
 };
+
+// The K-th largest of the keys every thread passes (0 = no key): the largest
+// r such that at least K keys are >= r, 0 if there are fewer than K keys.
+// Two bits per step, counted with warp ballots and one block barrier per
+// step.  Every thread calls it and gets the result.
 template <int KB>
-__device__ void block_kth_pair(uint32_t k0, uint32_t k1, unsigned K, RkPairRed &pr, uint32_t &r0, uint32_t &r1) {
+__device__ uint32_t block_kth_one(uint32_t k0, unsigned K, RkPairRed &pr) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    // step -1: how many keys each set has
-    unsigned h0 = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u)), h1 = (unsigned)__popc(__ballot_sync(kFull, k1 != 0u));
-    if (lane == 0) {
-        pr.c[1][wid][0] = h0;
-        pr.c[1][wid][1] = h1;
-    }
+    unsigned h = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u));
+    if (lane == 0) pr.c[1][wid][0] = h;
     __syncthreads();
-    h0 = h1 = 0u;
+    h = 0u;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) {
-        h0 += pr.c[1][w][0];
-        h1 += pr.c[1][w][1];
-    }
-    uint32_t a = 0u, b = 0u;  // the answers' bits fixed so far
+    for (int w = 0; w < kNW; ++w) h += pr.c[1][w][0];
+    if (h < K) return 0u;
+    uint32_t a = 0u;
     int par = 0;
 #pragma unroll 1
     for (int bit = KB - 2; bit >= 0; bit -= 2, par ^= 1) {
-        unsigned n[6];
+        unsigned n[3];
 #pragma unroll
-        for (int d = 1; d <= 3; ++d) {
-            n[d - 1] = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u && k0 >= (a | ((uint32_t)d << bit))));
-            n[d + 2] = (unsigned)__popc(__ballot_sync(kFull, k1 != 0u && k1 >= (b | ((uint32_t)d << bit))));
-        }
+        for (int d = 1; d <= 3; ++d) n[d - 1] = (unsigned)__popc(__ballot_sync(kFull, k0 != 0u && k0 >= (a | ((uint32_t)d << bit))));
         if (lane == 0)
 #pragma unroll
-            for (int j = 0; j < 6; ++j) pr.c[par][wid][j] = n[j];
+            for (int j = 0; j < 3; ++j) pr.c[par][wid][j] = n[j];
         __syncthreads();
-        // lane j < 6 sums count j over the warps; every lane takes the six sums
         unsigned mine = 0u;
-        if (lane < 6)
+        if (lane < 3)
 #pragma unroll
             for (int w = 0; w < kNW; ++w) mine += pr.c[par][w][lane];
-        unsigned t[6];
-#pragma unroll
-        for (int j = 0; j < 6; ++j) t[j] = __shfl_sync(kFull, mine, j);
-        a |= (t[2] >= K ? 3u : t[1] >= K ? 2u : t[0] >= K ? 1u : 0u) << bit;
-        b |= (t[5] >= K ? 3u : t[4] >= K ? 2u : t[3] >= K ? 1u : 0u) << bit;
+        const unsigned t0 = __shfl_sync(kFull, mine, 0), t1 = __shfl_sync(kFull, mine, 1), t2 = __shfl_sync(kFull, mine, 2);
+        a |= (t2 >= K ? 3u : t1 >= K ? 2u : t0 >= K ? 1u : 0u) << bit;
     }
-    r0 = h0 >= K ? a : 0u;
-    r1 = h1 >= K ? b : 0u;
-}
-
-// Writes the flagged entries (up to two per thread) to dst in thread order,
-// keeping at most `cap`; returns how many were flagged.  Every thread calls
-// it; the entries must already be in registers (dst may be their source).
-__device__ __forceinline__ int block_compact2(uint2 *dst, int cap, uint2 e0, bool f0, uint2 e1, bool f1, RkRed &rd) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const unsigned lt = lanemask_lt();
-    const unsigned b0 = __ballot_sync(kFull, f0), b1 = __ballot_sync(kFull, f1);
-    if (lane == 0) rd.u[0][wid] = (unsigned)(__popc(b0) + __popc(b1));
-    __syncthreads();  // (also: every thread has read its entries)
-    unsigned base = 0u, tot = 0u;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) {
-        const unsigned c = rd.u[0][w];
-        base += w < wid ? c : 0u;
-        tot += c;
-    }
-    const unsigned p0 = base + (unsigned)__popc(b0 & lt);
-    const unsigned p1 = base + (unsigned)__popc(b0) + (unsigned)__popc(b1 & lt);
-    if (f0 && p0 < (unsigned)cap) dst[p0] = e0;
-    if (f1 && p1 < (unsigned)cap) dst[p1] = e1;
-    __syncthreads();
-    return (int)tot;
+    return a;
 }
 
 // block dd sum of one term per thread, in a fixed order (every thread gets it)
@@ -639,33 +558,14 @@ struct RkRowView {
         nhead = sp.body0 - sp.head0;
         ntail = sp.hi - sp.tail0;
     }
-    __device__ __forceinline__ void prefetch_group(int c) const {
-        const uint32_t off = (uint32_t)c * kRkCH;
-        const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
-#pragma unroll
-        for (int i = 0; i < kRkVec; ++i) {
-            const int qv = (int)threadIdx.x + i * kNT;
-            if (qv < nv) prefetch_l2(body + (int64_t)c * (kRkCH / 16) + qv);
-        }
-    }
-    // group (chunk c, thread t): its vectors, -inf past the body
+    // group (chunk c, thread t): its vectors, -inf past the body (a chunk
+    // index past the row, from a pass that did not finish, reads nothing)
     __device__ __forceinline__ void load_group_of(int c, int t, uint4 (&v)[kRkVec]) const {
         const uint32_t off = (uint32_t)c * kRkCH;
         const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
 #pragma unroll
         for (int i = 0; i < kRkVec; ++i) {
             const int qv = t + i * kNT;
-            v[i] = qv < nv ? __ldg(body + (int64_t)c * (kRkCH / 16) + qv) : vec_neg_inf<T>();
-        }
-    }
-    // group (chunk c, this thread): its vectors, -inf past the body (a chunk
-    // index past the row, from a pass that did not finish, reads nothing)
-    __device__ __forceinline__ void load_group(int c, uint4 (&v)[kRkVec]) const {
-        const uint32_t off = (uint32_t)c * kRkCH;
-        const int nv = off < bytes ? (int)(min((uint32_t)kRkCH, bytes - off) / 16u) : 0;
-#pragma unroll
-        for (int i = 0; i < kRkVec; ++i) {
-            const int qv = (int)threadIdx.x + i * kNT;
             v[i] = qv < nv ? __ldg(body + (int64_t)c * (kRkCH / 16) + qv) : vec_neg_inf<T>();
         }
     }
@@ -686,26 +586,7 @@ __device__ __forceinline__ unsigned warp_reserve(unsigned n, int *cnt) {
     return __shfl_sync(kFull, base, 31) + incl - n;
 }
 
-// the elements of group c that reach tf (bits of hm), from `at` on
-template <typename T>
-__device__ __forceinline__ void write_group(uint2 *cand, unsigned &at, int body0, int c, const uint4 (&v)[kRkVec],
-                                            uint32_t hm) {
-    constexpr int VEC = Elem<T>::VEC;
-    constexpr int ECH = kRkCH / (int)sizeof(T);
-    const int vbase = body0 + c * ECH;
-#pragma unroll
-    for (int i = 0; i < kRkVec; ++i) {
-        uint32_t h = (hm >> (VEC * i)) & ((1u << VEC) - 1u);
-        while (h) {
-            const int e = __ffs(h) - 1;
-            h &= h - 1u;
-            if (at < (unsigned)kRkCap)
-                cand[at] = make_uint2(kkey<T>(vec_elem<T>(v[i], e)), (uint32_t)(vbase + ((int)threadIdx.x + i * kNT) * VEC + e));
-            ++at;
-        }
-    }
-}
-// the same for group (c, t) of another thread
+// the elements of group (chunk c, thread t) that reach tf (bits of hm), from `at` on
 template <typename T>
 __device__ __forceinline__ void write_group_of(uint2 *cand, unsigned &at, int body0, int c, int t, const uint4 (&v)[kRkVec],
                                                uint32_t hm) {
@@ -733,180 +614,142 @@ __device__ __forceinline__ uint32_t group_hits(const uint4 (&v)[kRkVec], float t
     return hm;
 }
 
-// The decision: one block per position.
+// The decision: one block per row.  A row's block takes its row's threshold
+// bound, reloads its candidate groups and builds its kept set; for the two
+// rows of a position the block that arrives second (one counter per
+// position) reads the other row's published kept set and decides.
 template <typename T>
-__global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams p) {
+__global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_decide_kernel(SampleParams p) {
+    constexpr int KB = Elem<T>::KEY_BITS;
     __shared__ SampBase sb;
     __shared__ RkRed rd;
-    __shared__ int s_cnt[2];  // candidates listed per row (may pass kRkCap: then some were lost)
-    __shared__ int s_ng;      // candidate groups of the position
-    __shared__ uint32_t glist[kRkGroupCap];  // (row << 31 | chunk << 8 | owner thread)
-    __shared__ RkInputs s_in;
     __shared__ RkPairRed pr;
     __shared__ __align__(16) float4 s_red4[kNW];
+    __shared__ int s_cnt;    // candidates listed (may pass kRkCap: then some were lost)
+    __shared__ int s_ng;     // candidate groups of the row
+    __shared__ unsigned s_last;
+    __shared__ RkInputs s_in;
+    __shared__ uint32_t glist[3 * kNT];  // (chunk << 8 | owner thread); at most three per pass thread
     extern __shared__ __align__(128) unsigned char dsm[];
     RkDecide &D = *reinterpret_cast<RkDecide *>(dsm);
-    uint2 *cand = reinterpret_cast<uint2 *>(dsm + kRkCandOff);  // [2][kRkCap]
+    uint2 *cand = reinterpret_cast<uint2 *>(dsm + kRkCandOff);  // [kRkCap]
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const unsigned K = (unsigned)p.top_k;
-    const int g = p.gamma;
-    const int pos = blockIdx.x, b = pos / (g + 1), k = pos - b * (g + 1);
-    const int rows = k < g ? 2 : 1;
+    const int g = p.gamma, B = p.B;
     const bool nucleus = p.top_p > 0.0f && p.top_p < 1.0f;
+    // row q: position-major, a position's target row then its draft row (as the pass)
+    const int q = blockIdx.x;
+    int k, b, r;
+    if (q < 2 * B * g) {
+        k = q / (2 * B);
+        const int rem = q - k * 2 * B;
+        b = rem >> 1;
+        r = rem & 1;
+    } else {
+        k = g;
+        b = q - 2 * B * g;
+        r = 0;
+    }
+    const int pos = b * (g + 1) + k;
     load_exp_tables(p, sb);
     const DdExpTables &EK = sb.K;
-    if (tid < 2) s_cnt[tid] = 0;
-    if (tid == 0) s_ng = 0;
-    // what does not depend on the pass: the position's inputs, the rows'
-    // head and tail scalars
     if (tid == 0) {
+        s_cnt = 0;
+        s_ng = 0;
         s_in.d = k < g ? p.tokens[(int64_t)b * g + k] : 0;
         s_in.u_k = k < g ? p.unif[(int64_t)b * (g + 1) + k] : 0.0f;
         s_in.u_f = p.unif[(int64_t)b * (g + 1) + g];
     }
-    const RkRowView<T> V0(reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride, p.V);
-    const RkRowView<T> V1(k < g ? reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride
-                                : reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride, p.V);
-    float xh[2], xt[2];
-    xh[0] = tid < V0.nhead ? ld_elem(V0.row, V0.head0 + tid) : -INFINITY;
-    xt[0] = tid < V0.ntail ? ld_elem(V0.row, V0.tail0 + tid) : -INFINITY;
-    xh[1] = rows > 1 && tid < V1.nhead ? ld_elem(V1.row, V1.head0 + tid) : -INFINITY;
-    xt[1] = rows > 1 && tid < V1.ntail ? ld_elem(V1.row, V1.tail0 + tid) : -INFINITY;
+    const RkRowView<T> W(r == 0 ? reinterpret_cast<const T *>(p.target) + (int64_t)pos * p.tstride
+                                : reinterpret_cast<const T *>(p.draft) + (int64_t)(b * g + k) * p.dstride,
+                         p.V);
+    const float xh = tid < W.nhead ? ld_elem(W.row, W.head0 + tid) : -INFINITY;
+    const float xt = tid < W.ntail ? ld_elem(W.row, W.tail0 + tid) : -INFINITY;
 
-    pdl_wait_primary();  // the pass's results (and this call's rejection words) from here on
-    const unsigned rejw = tid == 0 ? *((volatile unsigned *)&p.rejword[b]) : 0u;
-    uint32_t km[2] = {0u, 0u}, t4[2][4];
+    pdl_wait_primary();  // the pass's results from here on
+    const int64_t slot = (int64_t)pos * 2 + r;
+    const uint32_t km = __ldcg(p.rkmax + slot * kNT + tid);
+    uint32_t t4[4];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        const int64_t slot = (int64_t)pos * 2 + rr;
-        const bool on = rr < rows;
-        km[rr] = on ? __ldcg(p.rkmax + slot * kNT + tid) : 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) t4[rr][j] = on ? __ldcg(p.rkgrp + (slot * 4 + j) * kNT + tid) : 0u;
-    }
-    if (tid == 0) s_in.rej = rejw;
-    // theta per row: the K-th largest thread maximum (0 with fewer than K
-    // finite ones: every group is listed, the kept set is every finite logit)
-    constexpr int KB = Elem<T>::KEY_BITS;
-    uint32_t th16[2], theta[2];
-    float tf[2];
-    block_kth_pair<KB>(km[0], km[1], K, pr, theta[0], theta[1]);
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        th16[rr] = theta[rr] >> (KB - 16);
-        tf[rr] = fmaxf(key_value<T>(theta[rr]), lowest_finite<T>());
-    }
-    auto is_cand = [&](int rr, uint32_t t) { return t != 0u && (t >> 16) >= th16[rr]; };
+    for (int j = 0; j < 4; ++j) t4[j] = __ldcg(p.rkgrp + (slot * 4 + j) * kNT + tid);
+    // theta: the K-th largest thread maximum (0 with fewer than K finite
+    // ones: every group is listed, the kept set is every finite logit)
+    const uint32_t theta = block_kth_one<KB>(km, K, pr);
+    const uint32_t th16 = theta >> (KB - 16);
+    const float tf = fmaxf(key_value<T>(theta), lowest_finite<T>());
+    auto is_cand = [&](uint32_t t) { return t != 0u && (t >> 16) >= th16; };
     // a thread whose fourth group qualifies may have more: the exact path
-    const bool over = is_cand(0, t4[0][3]) || (rows > 1 && is_cand(1, t4[1][3]));
-    bool exact = __syncthreads_or(over);  // block-uniform
-    if (!exact) {
-        // ---- the listing ----
-        // 1. the candidate groups of both rows, (row, chunk, owner thread),
-        //    into one shared list; 2. one group per thread: its vectors
-        //    reloaded (all in flight at once) and its elements >= tf listed.
-        //    The head and tail scalars are listed by their own threads.
-        {
-            unsigned ng = 0u;
+    bool ovf = __syncthreads_or(is_cand(t4[3]));  // block-uniform
+    int count = 0;
+    if (!ovf) {
+        // ---- the listing: the candidate groups into a shared list, then
+        // one group per thread (the reloads all in flight at once); the head
+        // and tail scalars by their own threads ----
+        unsigned ng = 0u;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
+        for (int j = 0; j < 3; ++j) ng += is_cand(t4[j]) ? 1u : 0u;
+        unsigned at = warp_reserve(ng, &s_ng);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) ng += (rr < rows && is_cand(rr, t4[rr][j])) ? 1u : 0u;
-            unsigned at = warp_reserve(ng, &s_ng);
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-                    if (rr < rows && is_cand(rr, t4[rr][j])) {
-                        if (at < (unsigned)kRkGroupCap)
-                            glist[at] = ((uint32_t)rr << 31) | ((t4[rr][j] & 0xffffu) << 8) | (uint32_t)tid;
-                        ++at;
-                    }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                if (rr >= rows) break;  // block-uniform
-                const RkRowView<T> &W = rr ? V1 : V0;
-                const bool hh = xh[rr] >= tf[rr], ht = xt[rr] >= tf[rr];
-                unsigned ah = warp_reserve((hh ? 1u : 0u) + (ht ? 1u : 0u), &s_cnt[rr]);
-                uint2 *cb = cand + rr * kRkCap;
-                if (hh) {
-                    if (ah < (unsigned)kRkCap) cb[ah] = make_uint2(kkey<T>(xh[rr]), (uint32_t)(W.head0 + tid));
-                    ++ah;
-                }
-                if (ht && ah < (unsigned)kRkCap) cb[ah] = make_uint2(kkey<T>(xt[rr]), (uint32_t)(W.tail0 + tid));
-            }
+        for (int j = 0; j < 3; ++j)
+            if (is_cand(t4[j])) glist[at++] = ((t4[j] & 0xffffu) << 8) | (uint32_t)tid;
+        const bool hh = xh >= tf, ht = xt >= tf;
+        unsigned ah = warp_reserve((hh ? 1u : 0u) + (ht ? 1u : 0u), &s_cnt);
+        if (hh) {
+            if (ah < (unsigned)kRkCap) cand[ah] = make_uint2(kkey<T>(xh), (uint32_t)(W.head0 + tid));
+            ++ah;
         }
+        if (ht && ah < (unsigned)kRkCap) cand[ah] = make_uint2(kkey<T>(xt), (uint32_t)(W.tail0 + tid));
         __syncthreads();
-        {
-            const int ngr = min(s_ng, kRkGroupCap);
-            for (int g0 = 0; g0 < ngr; g0 += kNT) {  // (block-uniform trip count)
-                const int gi = g0 + tid;
-                const bool on = gi < ngr;
-                const uint32_t ge = on ? glist[gi] : 0u;
-                const int rr = (int)(ge >> 31), c = (int)((ge >> 8) & 0xffffu), owner = (int)(ge & 0xffu);
-                uint4 v[kRkVec];
-                if (on) (rr ? V1 : V0).load_group_of(c, owner, v);
-                const float tfr = rr ? tf[1] : tf[0];
-                const uint32_t hm = on ? group_hits<T>(v, tfr) : 0u;
-                // slots per row: a warp reserves for each row its lanes' hits
-                const unsigned a0 = warp_reserve(rr == 0 ? (unsigned)__popc(hm) : 0u, &s_cnt[0]);
-                const unsigned a1 = warp_reserve(rr == 1 ? (unsigned)__popc(hm) : 0u, &s_cnt[1]);
-                if (hm) {
-                    unsigned a = rr ? a1 : a0;
-                    write_group_of<T>(cand + rr * kRkCap, a, (rr ? V1 : V0).body0, c, owner, v, hm);
-                }
-            }
-            // more candidate groups than the list holds: the exact path
-            if (s_ng > (unsigned)kRkGroupCap) s_cnt[0] = kRkCap + 1;
+        const int ngr = s_ng;  // <= 3 * kNT
+        for (int g0 = 0; g0 < ngr; g0 += kNT) {  // (block-uniform trip count)
+            const int gi = g0 + tid;
+            const bool on = gi < ngr;
+            const uint32_t ge = on ? glist[gi] : 0u;
+            const int c = (int)(ge >> 8), owner = (int)(ge & 0xffu);
+            uint4 v[kRkVec];
+            if (on) W.load_group_of(c, owner, v);
+            const uint32_t hm = on ? group_hits<T>(v, tf) : 0u;
+            unsigned a = warp_reserve((unsigned)__popc(hm), &s_cnt);
+            if (hm) write_group_of<T>(cand, a, W.body0, c, owner, v, hm);
         }
-        __syncthreads();  // every listed entry is in the buffers
+        __syncthreads();  // every listed entry is in the buffer
+        count = s_cnt;
+        ovf = count > kRkCap;  // block-uniform: candidates were lost
+    }
 
-        // ---- the kept sets: exact threshold, token order, statistics ----
-        // Half a block per row: thread t holds entries u, u + 128, ... of row
-        // t / 128 (u = t % 128).  An entry is kept iff fewer than K listed
-        // entries of its row are larger: exactly the entries >= the K-th
-        // largest (ties included).  Only warps holding entries scan the list.
-        constexpr int HALF = kNT / 2, HW = HALF / 32, PER = kRkCap / HALF;
-        const int rr = tid / HALF, u = tid % HALF;
-        int cnt[2];
-        bool ovf[2];
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            cnt[x] = x < rows ? s_cnt[x] : 0;
-            ovf[x] = cnt[x] > kRkCap;
-        }
-        const int n = ovf[rr] ? 0 : cnt[rr];
-        const uint2 *cb = cand + rr * kRkCap;
-        uint2 e[PER];
-        bool f[PER];
+    // ---- the kept set: an entry is kept iff fewer than K listed entries are
+    // larger, i.e. exactly the entries >= the K-th largest (ties included);
+    // token order by counting; maximum, threshold, double-float normaliser ----
+    int kn = 0;
+    uint32_t th = 0u;
+    float m = -INFINITY;
+    dd S{0.0f, 0.0f};
+    if (!ovf) {
+        const int n = count;
+        const uint2 e0 = tid < n ? cand[tid] : make_uint2(0u, 0u);
+        const uint2 e1 = tid + kNT < n ? cand[tid + kNT] : make_uint2(0u, 0u);
+        bool f0 = false, f1 = false;
         unsigned nk = 0u;
         uint32_t mx = 0u, lo = 0xffffffffu;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            e[i] = u + i * HALF < n ? cb[u + i * HALF] : make_uint2(0u, 0u);
-            f[i] = false;
-        }
-        if (__any_sync(kFull, u < n)) {
-            unsigned gr[PER] = {};
-            if (n <= HALF) {  // one entry per thread (the usual case)
+        if (__any_sync(kFull, tid < n)) {
+            unsigned g0 = 0u, g1 = 0u;
+            if (n <= kNT) {
 #pragma unroll 8
-                for (int y = 0; y < n; ++y) gr[0] += cb[y].x > e[0].x ? 1u : 0u;
+                for (int y = 0; y < n; ++y) g0 += cand[y].x > e0.x ? 1u : 0u;
             } else {
                 for (int y = 0; y < n; ++y) {
-                    const uint32_t ky = cb[y].x;
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) gr[i] += ky > e[i].x ? 1u : 0u;
+                    const uint32_t ky = cand[y].x;
+                    g0 += ky > e0.x ? 1u : 0u;
+                    g1 += ky > e1.x ? 1u : 0u;
                 }
             }
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                f[i] = e[i].x != 0u && gr[i] < K;
-                nk += f[i] ? 1u : 0u;
-                mx = max(mx, e[i].x);
-                if (f[i]) lo = min(lo, e[i].x);
-            }
+            f0 = e0.x != 0u && g0 < K;
+            f1 = e1.x != 0u && g1 < K;
+            nk = (f0 ? 1u : 0u) + (f1 ? 1u : 0u);
+            mx = max(e0.x, e1.x);
+            if (f0) lo = e0.x;
+            if (f1) lo = min(lo, e1.x);
         }
-        // per half: kept count, largest key, smallest kept key
         nk = __reduce_add_sync(kFull, nk);
         mx = __reduce_max_sync(kFull, mx);
         lo = __reduce_min_sync(kFull, lo);
@@ -915,87 +758,129 @@ __global__ void __launch_bounds__(kNT, 3) chain_topk_decide_kernel(SampleParams 
             rd.u[1][wid] = mx;
             pr.c[0][wid][0] = lo;
         }
-        unsigned char *kflag = reinterpret_cast<unsigned char *>(D.prb);  // [2][kRkCap] kept flags (free until top-p)
-        static_assert(sizeof(D.prb) >= 2 * kRkCap, "kept flags fit");
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if (u + i * HALF < n) kflag[rr * kRkCap + u + i * HALF] = f[i];
+        unsigned char *kflag = reinterpret_cast<unsigned char *>(D.prb);  // [kRkCap] kept flags (free until top-p)
+        static_assert(sizeof(D.prb) >= kRkCap, "kept flags fit");
+        if (tid < n) kflag[tid] = f0;
+        if (tid + kNT < n) kflag[tid + kNT] = f1;
         __syncthreads();
-        unsigned kn_r = 0u;
-        uint32_t mk_r = 0u, th_r = 0xffffffffu;
+        unsigned knu = 0u;
+        uint32_t mk = 0u, tl = 0xffffffffu;
 #pragma unroll
-        for (int w = 0; w < HW; ++w) {
-            kn_r += rd.u[0][rr * HW + w];
-            mk_r = max(mk_r, rd.u[1][rr * HW + w]);
-            th_r = min(th_r, pr.c[0][rr * HW + w][0]);
+        for (int w = 0; w < kNW; ++w) {
+            knu += rd.u[0][w];
+            mk = max(mk, rd.u[1][w]);
+            tl = min(tl, pr.c[0][w][0]);
         }
-        th_r = (unsigned)n >= K ? th_r : 0u;
-        const bool big = kn_r > (unsigned)kKeptMax;
-        // token order among the kept entries of the row; the normaliser's terms
-        const float m = kn_r > 0u ? key_value<T>(mk_r) : -INFINITY;
-        dd t{0.0f, 0.0f};
-        bool anyf = false;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) anyf = anyf || f[i];
-        if (!big && __any_sync(kFull, anyf)) {
-            unsigned rk[PER] = {};
-            const unsigned char *kf = kflag + rr * kRkCap;
-            if (n <= HALF) {
+        kn = (int)knu;
+        th = (unsigned)n >= K ? tl : 0u;
+        m = kn > 0 ? key_value<T>(mk) : -INFINITY;
+        if (kn > kKeptMax) {
+            ovf = true;  // block-uniform: hundreds of ties
+        } else {
+            dd t{0.0f, 0.0f};
+            if (__any_sync(kFull, f0 || f1)) {
+                unsigned r0 = 0u, r1 = 0u;
+                if (n <= kNT) {
 #pragma unroll 8
-                for (int y = 0; y < n; ++y) rk[0] += (kf[y] && cb[y].y < e[0].y) ? 1u : 0u;
-            } else {
-                for (int y = 0; y < n; ++y) {
-                    if (!kf[y]) continue;
-                    const uint32_t ty = cb[y].y;
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) rk[i] += ty < e[i].y ? 1u : 0u;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < PER; ++i)
-                if (f[i]) {
-                    D.kept[rr][rk[i]] = e[i];
-                    t = dd_add(t, dd_expw(key_value<T>(e[i].x), m, EK));
-                }
-        }
-        dd Sp[2] = {rr == 0 ? t : dd{0.0f, 0.0f}, rr == 1 ? t : dd{0.0f, 0.0f}};
-        if (u == 0) {  // one thread per half: the row's statistics
-            D.m[rr] = m;
-            D.kn[rr] = kn_r;
-            D.th[rr] = th_r;
-            if (rr == 0) D.ahit = 0u;
-        }
-        // both rows' normalisers in one block reduction (its barriers also
-        // publish D.kn, D.th, D.m); a kept set too large for the arrays, in
-        // either row, sends the position to the exact path
-        const bool anybig = __syncthreads_or(big);
-        block_dd_sum2<kNT>(Sp[0], Sp[1], s_red4);
-        if (anybig || ovf[0] || (rows > 1 && ovf[1])) exact = true;  // block-uniform
-        if (!exact) {
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                if (x >= rows) break;
-                dd S = Sp[x];
-                if (nucleus && D.m[x] != -INFINITY) {
-                    int knr = (int)D.kn[x];
-                    uint32_t thr = D.th[x];
-                    __syncthreads();  // the kept set is in place; every thread has read D.kn/th
-                    if (wid == 0) {
-                        row_top_p<T>(D.kept[x], knr, thr, D.m[x], S, p.top_p, D.tmp, D.prb, EK);
-                        if (lane == 0) {
-                            D.kn[x] = (unsigned)knr;
-                            D.th[x] = thr;
-                            D.S[x] = make_float2(S.hi, S.lo);
-                        }
+                    for (int y = 0; y < n; ++y) r0 += (kflag[y] && cand[y].y < e0.y) ? 1u : 0u;
+                } else {
+                    for (int y = 0; y < n; ++y) {
+                        if (!kflag[y]) continue;
+                        const uint32_t ty = cand[y].y;
+                        r0 += ty < e0.y ? 1u : 0u;
+                        r1 += ty < e1.y ? 1u : 0u;
                     }
-                } else if (tid == 0) {
-                    D.S[x] = make_float2(S.hi, S.lo);
+                }
+                if (f0) {
+                    D.kept[r][r0] = e0;
+                    t = dd_expw(key_value<T>(e0.x), m, EK);
+                }
+                if (f1) {
+                    D.kept[r][r1] = e1;
+                    t = dd_add(t, dd_expw(key_value<T>(e1.x), m, EK));
                 }
             }
+            S = block_dd_sum(t, rd);  // (its barriers also publish D.kept)
+            if (nucleus && m != -INFINITY) {
+                if (wid == 0) {
+                    row_top_p<T>(D.kept[r], kn, th, m, S, p.top_p, D.tmp, D.prb, EK);
+                    if (lane == 0) {
+                        D.kn[r] = (unsigned)kn;
+                        D.th[r] = th;
+                        D.S[r] = make_float2(S.hi, S.lo);
+                    }
+                }
+                __syncthreads();
+                kn = (int)D.kn[r];
+                th = D.th[r];
+                S = dd{D.S[r].x, D.S[r].y};
+            }
         }
-        __syncthreads();
     }
-    if (exact) {  // the decision arrays and buffers are free: the exact path's ring
+    __syncthreads();  // every thread has read D.kn/th/S above
+    if (tid == 0) {
+        D.kn[r] = (unsigned)kn;
+        D.th[r] = th;
+        D.m[r] = m;
+        D.S[r] = make_float2(S.hi, S.lo);
+        D.flags[r] = ovf ? 1u : 0u;
+    }
+    if (k < g) {  // publish for the position's other block
+        if (tid == 0) {
+            TopkRow h;
+            h.kn = (unsigned)kn;
+            h.th = th;
+            h.m = m;
+            h.s_hi = S.hi;
+            h.s_lo = S.lo;
+            h.flags = ovf ? 1u : 0u;
+            h.pad[0] = h.pad[1] = 0u;
+            p.rkrow[slot] = h;
+        }
+        if (!ovf && tid < kn) p.rkent[slot * kKeptMax + tid] = D.kept[r][tid];
+        __threadfence();
+    }
+    __syncthreads();
+    // ---- the position's decision, by the block that arrives last ----
+    if (tid == 0) {
+        unsigned last = 1u;
+        if (k < g) {
+            last = atomicAdd(p.rkcnt + pos, 1u) == 1u;
+            if (last) {
+                p.rkcnt[pos] = 0u;  // left zeroed for the next call
+                __threadfence();
+            }
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // one round of reads: the request's rejection word, the other row's
+    // header and every slot of its kept set (those past its count unused)
+    const unsigned rejw = tid == 0 ? *((volatile unsigned *)&p.rejword[b]) : 0u;
+    if (k < g) {
+        const int64_t ri = (int64_t)pos * 2 + (1 - r);
+        const uint4 *hp = reinterpret_cast<const uint4 *>(p.rkrow + ri);
+        const uint4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1);
+        const uint2 oe = __ldcg(p.rkent + ri * kKeptMax + tid);
+        const unsigned okn = h0.x;
+        if (tid == 0) {
+            D.kn[1 - r] = okn;
+            D.th[1 - r] = h0.y;
+            D.m[1 - r] = __uint_as_float(h0.z);
+            D.S[1 - r] = make_float2(__uint_as_float(h0.w), __uint_as_float(h1.x));
+            D.flags[1 - r] = h1.y;
+        }
+        if (!(h1.y & 1u) && tid < (int)okn) D.kept[1 - r][tid] = oe;
+    }
+    if (tid == 0) {
+        s_in.rej = rejw;
+        D.ahit = 0u;
+    }
+    __syncthreads();
+    const bool exact = ((D.flags[0] | (k < g ? D.flags[1] : 0u)) & 1u) != 0u;  // block-uniform
+    if (exact) {  // the decision arrays are free: the exact path's ring
+        __syncthreads();
         rk_exact_position<T>(p, sb, dsm, k, b);
     } else {
         const Outcome o = block_outcome<T>(p, b, k, D, EK, rd, s_red4, s_in);
@@ -1022,7 +907,7 @@ static cudaError_t launch_topk(const SampleParams &p, int sms, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)p.B * (p.gamma + 1)));
+    cfg.gridDim = dim3((unsigned)rows);  // one block per row
     cfg.blockDim = dim3(kNT);
     cfg.dynamicSmemBytes = kRkDecideDyn;
     cfg.stream = s;
