@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kNT, kRkBlocksPerSM) chain_topk_decide_kernel(
             p.rkrow[slot] = h;
         }
         if (!ovf && tid < kn) p.rkent[slot * kKeptMax + tid] = D.kept[r][tid];
-        __threadfence();
+        if (tid == 0 || (!ovf && tid < kn)) __threadfence();  // the writers' stores before the arrival
     }
     __syncthreads();
     // ---- the position's decision, by the block that arrives last ----
