@@ -1,5 +1,5 @@
 // Sampled chain verification with top-k (k <= 128) on sm_103a: a pass over
-// the logits, then one block per position.
+// the logits, then one decision block per row.
 //
 // The transform ("KV Cache 优化（四）：Speculative Decoding 投机解码" §4) keeps
 // every logit >= the row's k-th largest, so after one pass over a row only a
