@@ -86,10 +86,19 @@ def test_workspace_sizes(lib):
     assert L.spec_workspace_bytes(L.SPEC_WS_TREE, 128, 5, 128256) >= 256 + 128 * 4 + 128 * 5 * 8
     assert L.spec_workspace_bytes(L.SPEC_WS_COMMIT, 512, 0, 0) >= 256 + 512 * 4
     base = L.spec_workspace_bytes(L.SPEC_WS_CHAIN, 64, 4, 128256)
-    # the top-k path: per position two row slots, each with 256 thread maxima
-    # and 4 x 256 packed groups of 4 bytes
-    assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 64, 4, 128256) >= \
-        base + 64 * 5 * 2 * (256 * 4 + 4 * 256 * 4)
+    # the chain workspace exactly: a 256-byte header, two per-request words,
+    # a 16-byte record per position, each region rounded up to 256 bytes
+    al = lambda x: (x + 255) // 256 * 256
+    rows = 64 * 5
+    assert base == 256 + 2 * al(64 * 4) + al(rows * 16)
+    # the top-k path adds, per position and row slot: 256 thread maxima and
+    # 4 x 256 packed groups (4 bytes each) from the pass, then a 32-byte kept-set
+    # header and 256 kept entries of 8 bytes, and one arrival counter per
+    # position; none of it depends on V
+    topk = base + al(rows * 2 * 256 * 4) + al(rows * 2 * 4 * 256 * 4) + al(rows * 2 * 32) + \
+        al(rows * 2 * 256 * 8) + al(rows * 4)
+    assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 64, 4, 128256) == topk
+    assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN_TOPK, 64, 4, 1000) == topk
     assert L.spec_workspace_bytes(99, 1, 1, 1) == 0
     assert L.spec_workspace_bytes(L.SPEC_WS_CHAIN, -1, 1, 1) == 0
 
